@@ -1,0 +1,542 @@
+// pi_api.cu -- host side of the C ABI declared in include/pi_ffn.h.
+//
+// Validates every argument before launching anything, owns the workspace, and
+// chains the kernels of one decode step on the caller's stream: predictor
+// (K1 hidden, K2 logits + compaction) -> gate/up gather (K3) -> W_down axpy (K4a)
+// -> deterministic reduction (K4b). Kernels after the first of a call use
+// programmatic dependent launch so that their weight loads overlap the
+// previous kernel's tail. The layer stack is recorded into a CUDA graph.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "pi_ffn.h"
+#include "pi_internal.h"
+
+using namespace pi;
+
+namespace {
+
+constexpr float RMS_EPS = 1e-6f;
+
+typedef CUresult (*GetRangeFn)(CUdeviceptr *, size_t *, CUdeviceptr);
+
+GetRangeFn get_range_fn()
+{
+    static GetRangeFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (GetRangeFn)p;
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// A pointer the kernels may read or write `bytes` bytes at: non-NULL, aligned,
+// device (or managed) memory of device `dev`, and, where the driver can say,
+// inside one allocation.
+pi_status_t check_ptr(const void *p, size_t bytes, size_t align, int dev)
+{
+    if (!p || ((uintptr_t)p % align) != 0) return PI_ERR_INVALID_ARG;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return PI_ERR_INVALID_ARG;
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return PI_ERR_INVALID_ARG;
+    if (a.type == cudaMemoryTypeDevice && a.device != dev) return PI_ERR_INVALID_ARG;
+    if (GetRangeFn fn = get_range_fn()) {
+        CUdeviceptr base = 0;
+        size_t size = 0;
+        if (fn(&base, &size, (CUdeviceptr)(uintptr_t)p) == CUDA_SUCCESS) {
+            if ((uintptr_t)p + bytes > (uintptr_t)base + size) return PI_ERR_INVALID_ARG;
+        }
+    }
+    return PI_OK;
+}
+
+pi_status_t check_opt(const void *p, size_t bytes, size_t align, int dev)
+{
+    return p ? check_ptr(p, bytes, align, dev) : PI_OK;
+}
+
+size_t elt_row_bytes(int dt, int64_t n)
+{
+    switch (dt) {
+    case PI_F32: return (size_t)n * 4;
+    case PI_BF16:
+    case PI_F16: return (size_t)n * 2;
+    case PI_INT4_G128: return (size_t)n / 2;
+    }
+    return 0;
+}
+
+pi_status_t validate_desc(const pi_ffn_desc_t *d)
+{
+    if (!d) return PI_ERR_INVALID_ARG;
+    if (d->d < 8 || d->d % 8 || d->f < 1 || d->r < 8 || d->r % 8 || d->n_layers < 1 || d->max_batch < 1 ||
+        d->max_batch > 256)
+        return PI_ERR_INVALID_ARG;
+    if (d->kind != PI_FFN_GATED_RELU && d->kind != PI_FFN_RELU) return PI_ERR_INVALID_ARG;
+    if (d->wdtype < PI_F32 || d->wdtype > PI_INT4_G128) return PI_ERR_INVALID_ARG;
+    if (d->pdtype < PI_F32 || d->pdtype > PI_F16) return PI_ERR_INVALID_ARG;
+    if (!std::isfinite(d->tau_logit)) return PI_ERR_INVALID_ARG;
+    if (d->wdtype == PI_INT4_G128 && d->d % 128) return PI_ERR_UNSUPPORTED;
+    // one batch row of the staged input vector must fit the shared-memory budget
+    if ((size_t)d->d * 4 > SMEM_VEC_CAP || (size_t)d->r * 4 > SMEM_VEC_CAP) return PI_ERR_UNSUPPORTED;
+    if (d->f > (1 << 26)) return PI_ERR_UNSUPPORTED;
+    return PI_OK;
+}
+
+// Largest batch tile (1, 2, 4 or 8) whose fp32 vectors of length K fit the budget, capped near B.
+int pick_bt(int B, int K, int cap = 8)
+{
+    int fit = (int)(SMEM_VEC_CAP / ((size_t)K * 4));
+    int bt = 1;
+    while (bt * 2 <= cap && bt * 2 <= fit && bt < B) bt *= 2;
+    return bt;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+struct pi_ffn {
+    pi_ffn_desc_t desc;
+    std::vector<pi_layer_weights_t> layers;
+    int dev = 0, nsm = 0;
+    void *ws = nullptr;
+    float *xbuf[2] = {nullptr, nullptr};
+    float *inv_rms = nullptr, *sumsq = nullptr, *hp = nullptr, *hbuf = nullptr, *part = nullptr;
+    uint32_t *maskw = nullptr, *tickets = nullptr, *status = nullptr;
+    int32_t *idx_ws = nullptr, *count_ws = nullptr, *counts_ws = nullptr;
+    // per-kernel event brackets (pi_profile_begin / pi_profile_end)
+    bool prof = false;
+    std::vector<cudaEvent_t> prof_ev;   // pairs: [2k] before, [2k+1] after launch k
+    std::vector<int> prof_kind;
+    size_t prof_n = 0;
+    // recorded decode step
+    cudaGraphExec_t gexec = nullptr;
+    int g_B = 0;
+    const float *g_x0 = nullptr;
+    float *g_xout = nullptr;
+    int32_t *g_counts = nullptr, *g_idx = nullptr;
+};
+
+namespace {
+
+pi_status_t cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return PI_OK;
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? PI_ERR_OOM : PI_ERR_CUDA;
+}
+
+pi_status_t validate_layer(const pi_ffn_t *h, const pi_layer_weights_t &w)
+{
+    const pi_ffn_desc_t &D = h->desc;
+    const size_t wrow = elt_row_bytes(D.wdtype, D.d), prow = elt_row_bytes(D.pdtype, D.d),
+                 p2row = elt_row_bytes(D.pdtype, D.r);
+    const size_t srow = (size_t)(D.d / 128) * 2;
+    const bool gated = D.kind == PI_FFN_GATED_RELU, int4 = D.wdtype == PI_INT4_G128;
+    pi_status_t s;
+    if ((s = check_ptr(w.w_gate, wrow * D.f, 16, h->dev))) return s;
+    if ((s = check_ptr(w.w_down_t, wrow * D.f, 16, h->dev))) return s;
+    if (gated) {
+        if ((s = check_ptr(w.w_up, wrow * D.f, 16, h->dev))) return s;
+    } else if (w.w_up || w.s_up) {
+        return PI_ERR_INVALID_ARG;
+    }
+    if (int4) {
+        if ((s = check_ptr(w.s_gate, srow * D.f, 2, h->dev))) return s;
+        if ((s = check_ptr(w.s_down, srow * D.f, 2, h->dev))) return s;
+        if (gated && (s = check_ptr(w.s_up, srow * D.f, 2, h->dev))) return s;
+    } else if (w.s_gate || w.s_up || w.s_down) {
+        return PI_ERR_INVALID_ARG;
+    }
+    if ((s = check_opt(w.b_gate, (size_t)D.f * 4, 4, h->dev))) return s;
+    if ((s = check_ptr(w.p1_t, prow * D.r, 16, h->dev))) return s;
+    if ((s = check_ptr(w.p2_t, p2row * D.f, 16, h->dev))) return s;
+    if ((s = check_opt(w.b_pred, (size_t)D.f * 4, 4, h->dev))) return s;
+    return PI_OK;
+}
+
+Launch mk(const pi_ffn_t *h, dim3 grid, size_t smem, cudaStream_t s, bool pdl)
+{
+    Launch L;
+    L.grid = grid;
+    L.block = dim3(NT);
+    L.smem = smem;
+    L.stream = s;
+    L.pdl = pdl;
+    L.nsm = h->nsm;
+    return L;
+}
+
+// Event bracket around one launch when profiling (no-op otherwise).
+struct ProfScope {
+    pi_ffn_t *h;
+    cudaStream_t s;
+    size_t slot;
+    ProfScope(const pi_ffn_t *hc, cudaStream_t st, int kind) : h(const_cast<pi_ffn_t *>(hc)), s(st), slot(0)
+    {
+        if (!h->prof) return;
+        slot = h->prof_n++;
+        while (h->prof_ev.size() < 2 * h->prof_n) {
+            cudaEvent_t e;
+            if (cudaEventCreate(&e) != cudaSuccess) {
+                cudaGetLastError();
+                h->prof = false;
+                return;
+            }
+            h->prof_ev.push_back(e);
+        }
+        if (h->prof_kind.size() < h->prof_n) h->prof_kind.resize(h->prof_n);
+        h->prof_kind[slot] = kind;
+        cudaEventRecord(h->prof_ev[2 * slot], s);
+    }
+    ~ProfScope()
+    {
+        if (h->prof && 2 * slot + 1 < h->prof_ev.size()) cudaEventRecord(h->prof_ev[2 * slot + 1], s);
+    }
+};
+
+// K1 + K2 for one layer. pdl_first: whether the first kernel may overlap its predecessor.
+cudaError_t enqueue_predict(const pi_ffn_t *h, int layer, const float *x, const float *inv_rms, int B,
+                            int32_t *idx, int32_t *count, cudaStream_t s, bool pdl_first)
+{
+    const pi_ffn_desc_t &D = h->desc;
+    const pi_layer_weights_t &w = h->layers[layer];
+    const int bt1 = pick_bt(B, D.d), bt2 = pick_bt(B, D.r);
+    const bool pdl = !h->prof;
+    cudaError_t e;
+    {
+        ProfScope p(h, s, PI_K_PRED_HIDDEN);
+        e = launch_pred_hidden(
+            mk(h, dim3((D.r + PRED_ROWS_HIDDEN - 1) / PRED_ROWS_HIDDEN), (size_t)bt1 * D.d * 4, s, pdl && pdl_first),
+            D.pdtype, bt1, w.p1_t, D.d, D.r, x, inv_rms, B, h->hp);
+    }
+    if (e != cudaSuccess) return e;
+    ProfScope p(h, s, PI_K_PRED_LOGITS);
+    return launch_pred_logits(
+        mk(h, dim3((D.f + PRED_ROWS_LOGIT - 1) / PRED_ROWS_LOGIT), (size_t)bt2 * D.r * 4, s, pdl), D.pdtype, bt2,
+        w.p2_t, D.r, D.f, w.b_pred, D.tau_logit, h->hp, B, h->maskw, h->tickets + 0, idx, count);
+}
+
+// K3 + K4a + K4b for one layer. xin != NULL: stack glue (out = xin + y, inv_rms for the next layer).
+cudaError_t enqueue_ffn(const pi_ffn_t *h, int layer, const float *x, const float *inv_rms, int B,
+                        const int32_t *idx, const int32_t *count, const float *xin, float *out, cudaStream_t s,
+                        bool pdl_first)
+{
+    const pi_ffn_desc_t &D = h->desc;
+    const pi_layer_weights_t &w = h->layers[layer];
+    const int bt = pick_bt(B, D.d);
+    const bool pdl = !h->prof;
+    cudaError_t e;
+    {
+        ProfScope p(h, s, PI_K_FFN_H);
+        e = launch_ffn_h(mk(h, dim3(0), (size_t)bt * D.d * 4, s, pdl && pdl_first), D.wdtype, D.kind, bt, w.w_gate,
+                         w.w_up, w.s_gate, w.s_up, w.b_gate, D.d, D.f, x, inv_rms, B, idx, count, h->hbuf, D.f,
+                         h->status);
+    }
+    if (e != cudaSuccess) return e;
+    const int btd = pick_bt(B, 1, D.wdtype == PI_INT4_G128 ? 2 : 8);
+    {
+        ProfScope p(h, s, PI_K_FFN_DOWN);
+        e = launch_ffn_down(mk(h, dim3(0), 0, s, pdl), D.wdtype, btd, w.w_down_t, w.s_down, D.d, D.f, idx, count,
+                            h->hbuf, D.f, B, h->part, h->status);
+    }
+    if (e != cudaSuccess) return e;
+    const dim3 rg((D.d + RED_COLS - 1) / RED_COLS, B);
+    ProfScope p(h, s, PI_K_REDUCE);
+    return launch_reduce(mk(h, rg, 0, s, pdl), h->part, D.d, B, D.f, count, xin, out, h->sumsq, h->tickets + 1,
+                         h->inv_rms, RMS_EPS);
+}
+
+cudaError_t enqueue_stack(const pi_ffn_t *h, const float *x0, int B, float *x_out, int32_t *counts,
+                          int32_t *idx_out, cudaStream_t s)
+{
+    const pi_ffn_desc_t &D = h->desc;
+    cudaError_t e;
+    {
+        ProfScope p(h, s, PI_K_RMS);
+        e = launch_rms(mk(h, dim3(B), 0, s, false), x0, D.d, B, h->inv_rms, RMS_EPS);
+    }
+    if (e != cudaSuccess) return e;
+    for (int l = 0; l < D.n_layers; ++l) {
+        const float *xl = l == 0 ? x0 : h->xbuf[(l - 1) & 1];
+        float *xn = l == D.n_layers - 1 ? x_out : h->xbuf[l & 1];
+        int32_t *idx = idx_out ? idx_out + (size_t)l * D.f : h->idx_ws;
+        int32_t *cnt = counts ? counts + l : h->counts_ws + l;
+        if ((e = enqueue_predict(h, l, xl, h->inv_rms, B, idx, cnt, s, true)) != cudaSuccess) return e;
+        if ((e = enqueue_ffn(h, l, xl, h->inv_rms, B, idx, cnt, xl, xn, s, true)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+bool legacy_stream(cudaStream_t s) { return s == nullptr || s == cudaStreamLegacy; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t pi_abi_version(void) { return PI_FFN_ABI_VERSION; }
+
+const char *pi_status_string(pi_status_t s)
+{
+    switch (s) {
+    case PI_OK: return "ok";
+    case PI_ERR_INVALID_ARG: return "invalid argument";
+    case PI_ERR_UNSUPPORTED: return "unsupported";
+    case PI_ERR_CUDA: return "CUDA error";
+    case PI_ERR_OOM: return "out of device memory";
+    case PI_ERR_TIMEOUT: return "device-side wait timed out";
+    case PI_ERR_DEVICE_CHECK: return "device-side input check failed";
+    }
+    return "unknown status";
+}
+
+pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_layer_weights_t *layers)
+{
+    if (!out) return PI_ERR_INVALID_ARG;
+    *out = nullptr;
+    pi_status_t s = validate_desc(desc);
+    if (s != PI_OK) return s;
+    if (!layers) return PI_ERR_INVALID_ARG;
+
+    pi_ffn_t *h = new (std::nothrow) pi_ffn_t();
+    if (!h) return PI_ERR_OOM;
+    h->desc = *desc;
+    h->layers.assign(layers, layers + desc->n_layers);
+    if ((s = cuda_status(cudaGetDevice(&h->dev))) != PI_OK ||
+        (s = cuda_status(cudaDeviceGetAttribute(&h->nsm, cudaDevAttrMultiProcessorCount, h->dev))) != PI_OK) {
+        delete h;
+        return s;
+    }
+    for (int l = 0; l < desc->n_layers; ++l) {
+        if ((s = validate_layer(h, h->layers[l])) != PI_OK) {
+            delete h;
+            return s;
+        }
+    }
+
+    const pi_ffn_desc_t &D = h->desc;
+    const size_t mb = (size_t)D.max_batch;
+    const size_t nred = (size_t)(D.d + RED_COLS - 1) / RED_COLS;
+    const size_t sizes[] = {
+        mb * D.d * 4, mb * D.d * 4,                    // xbuf[2]
+        mb * 4,                                        // inv_rms
+        nred * mb * 4,                                 // sumsq
+        mb * D.r * 4,                                  // hp
+        mb * D.f * 4,                                  // hbuf
+        (size_t)MAX_GROUPS * mb * D.d * 4,             // part
+        (size_t)(D.f + 31) / 32 * 4,                   // maskw
+        4 * 4,                                         // tickets
+        4,                                             // status
+        (size_t)D.f * 4,                               // idx_ws
+        4,                                             // count_ws
+        (size_t)D.n_layers * 4,                        // counts_ws
+    };
+    const int nbuf = sizeof(sizes) / sizeof(sizes[0]);
+    size_t off[16], total = 0;
+    for (int i = 0; i < nbuf; ++i) {
+        off[i] = total;
+        total = align_up(total + sizes[i], 256);
+    }
+    if ((s = cuda_status(cudaMalloc(&h->ws, total))) != PI_OK) {
+        delete h;
+        return s;
+    }
+    if ((s = cuda_status(cudaMemset(h->ws, 0, total))) != PI_OK) {
+        cudaFree(h->ws);
+        delete h;
+        return s;
+    }
+    char *base = (char *)h->ws;
+    h->xbuf[0] = (float *)(base + off[0]);
+    h->xbuf[1] = (float *)(base + off[1]);
+    h->inv_rms = (float *)(base + off[2]);
+    h->sumsq = (float *)(base + off[3]);
+    h->hp = (float *)(base + off[4]);
+    h->hbuf = (float *)(base + off[5]);
+    h->part = (float *)(base + off[6]);
+    h->maskw = (uint32_t *)(base + off[7]);
+    h->tickets = (uint32_t *)(base + off[8]);
+    h->status = (uint32_t *)(base + off[9]);
+    h->idx_ws = (int32_t *)(base + off[10]);
+    h->count_ws = (int32_t *)(base + off[11]);
+    h->counts_ws = (int32_t *)(base + off[12]);
+    *out = h;
+    return PI_OK;
+}
+
+void pi_ffn_destroy(pi_ffn_t *h)
+{
+    if (!h) return;
+    cudaDeviceSynchronize();
+    if (h->gexec) cudaGraphExecDestroy(h->gexec);
+    for (cudaEvent_t e : h->prof_ev) cudaEventDestroy(e);
+    if (h->ws) cudaFree(h->ws);
+    cudaGetLastError();
+    delete h;
+}
+
+pi_status_t pi_predict(pi_ffn_t *h, int32_t layer, const float *u, int32_t B, int32_t *idx, int32_t *count,
+                       void *stream)
+{
+    if (!h || layer < 0 || layer >= h->desc.n_layers || B < 1 || B > h->desc.max_batch) return PI_ERR_INVALID_ARG;
+    const pi_ffn_desc_t &D = h->desc;
+    pi_status_t s;
+    if ((s = check_ptr(u, (size_t)B * D.d * 4, 16, h->dev))) return s;
+    if ((s = check_ptr(idx, (size_t)D.f * 4, 4, h->dev))) return s;
+    if ((s = check_ptr(count, 4, 4, h->dev))) return s;
+    return cuda_status(enqueue_predict(h, layer, u, nullptr, B, idx, count, (cudaStream_t)stream, false));
+}
+
+pi_status_t pi_sparse_ffn(pi_ffn_t *h, int32_t layer, const float *u, int32_t B, const int32_t *idx,
+                          const int32_t *count, float *y, void *stream)
+{
+    if (!h || layer < 0 || layer >= h->desc.n_layers || B < 1 || B > h->desc.max_batch) return PI_ERR_INVALID_ARG;
+    const pi_ffn_desc_t &D = h->desc;
+    pi_status_t s;
+    if ((s = check_ptr(u, (size_t)B * D.d * 4, 16, h->dev))) return s;
+    if ((s = check_ptr(idx, 4, 4, h->dev))) return s;      // length is *count, checked on the device
+    if ((s = check_ptr(count, 4, 4, h->dev))) return s;
+    if ((s = check_ptr(y, (size_t)B * D.d * 4, 16, h->dev))) return s;
+    return cuda_status(enqueue_ffn(h, layer, u, nullptr, B, idx, count, nullptr, y, (cudaStream_t)stream, false));
+}
+
+pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_out, int32_t *counts,
+                            int32_t *idx_out, void *stream)
+{
+    if (!h || B < 1 || B > h->desc.max_batch) return PI_ERR_INVALID_ARG;
+    const pi_ffn_desc_t &D = h->desc;
+    pi_status_t s;
+    if ((s = check_ptr(x0, (size_t)B * D.d * 4, 16, h->dev))) return s;
+    if ((s = check_ptr(x_out, (size_t)B * D.d * 4, 16, h->dev))) return s;
+    if ((s = check_opt(counts, (size_t)D.n_layers * 4, 4, h->dev))) return s;
+    if ((s = check_opt(idx_out, (size_t)D.n_layers * D.f * 4, 4, h->dev))) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (!legacy_stream(st) && cudaStreamIsCapturing(st, &cs) != cudaSuccess) return cuda_status(cudaGetLastError());
+    if (legacy_stream(st) || cs != cudaStreamCaptureStatusNone || h->prof)
+        return cuda_status(enqueue_stack(h, x0, B, x_out, counts, idx_out, st));
+
+    if (!(h->gexec && h->g_B == B && h->g_x0 == x0 && h->g_xout == x_out && h->g_counts == counts &&
+          h->g_idx == idx_out)) {
+        if (h->gexec) {
+            cudaGraphExecDestroy(h->gexec);
+            h->gexec = nullptr;
+        }
+        cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeRelaxed);
+        if (e != cudaSuccess) return cuda_status(e);
+        cudaError_t el = enqueue_stack(h, x0, B, x_out, counts, idx_out, st);
+        cudaGraph_t g = nullptr;
+        e = cudaStreamEndCapture(st, &g);
+        if (el != cudaSuccess || e != cudaSuccess) {
+            if (g) cudaGraphDestroy(g);
+            return cuda_status(el != cudaSuccess ? el : e);
+        }
+        e = cudaGraphInstantiate(&h->gexec, g, 0);
+        cudaGraphDestroy(g);
+        if (e != cudaSuccess) {
+            h->gexec = nullptr;
+            return cuda_status(e);
+        }
+        h->g_B = B;
+        h->g_x0 = x0;
+        h->g_xout = x_out;
+        h->g_counts = counts;
+        h->g_idx = idx_out;
+    }
+    return cuda_status(cudaGraphLaunch(h->gexec, st));
+}
+
+pi_status_t pi_profile_begin(pi_ffn_t *h)
+{
+    if (!h) return PI_ERR_INVALID_ARG;
+    h->prof = true;
+    h->prof_n = 0;
+    return PI_OK;
+}
+
+pi_status_t pi_profile_end(pi_ffn_t *h, float *ms, int32_t *launches, int32_t n_kinds)
+{
+    if (!h || n_kinds < 0) return PI_ERR_INVALID_ARG;
+    const bool was = h->prof;
+    h->prof = false;
+    for (int k = 0; k < n_kinds; ++k) {
+        if (ms) ms[k] = 0.f;
+        if (launches) launches[k] = 0;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) return cuda_status(cudaGetLastError());
+    if (!was) return PI_OK;
+    for (size_t i = 0; i < h->prof_n && 2 * i + 1 < h->prof_ev.size(); ++i) {
+        const int k = h->prof_kind[i];
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, h->prof_ev[2 * i], h->prof_ev[2 * i + 1]) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (k >= 0 && k < n_kinds) {
+            if (ms) ms[k] += t;
+            if (launches) launches[k] += 1;
+        }
+    }
+    h->prof_n = 0;
+    return PI_OK;
+}
+
+pi_status_t pi_get_status(pi_ffn_t *h)
+{
+    if (!h) return PI_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return cuda_status(cudaGetLastError());
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, h->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_status(cudaGetLastError());
+    if (v && cudaMemset(h->status, 0, 4) != cudaSuccess) return cuda_status(cudaGetLastError());
+    return (pi_status_t)v;
+}
+
+pi_status_t pi_hot_first_order(const uint32_t *counts, int32_t f, int32_t *perm, void *stream)
+{
+    if (f < 0) return PI_ERR_INVALID_ARG;
+    if (f == 0) return PI_OK;
+    int dev = 0;
+    pi_status_t s;
+    if ((s = cuda_status(cudaGetDevice(&dev)))) return s;
+    if ((s = check_ptr(counts, (size_t)f * 4, 4, dev))) return s;
+    if ((s = check_ptr(perm, (size_t)f * 4, 4, dev))) return s;
+    return cuda_status(launch_hot_first(counts, f, perm, (cudaStream_t)stream));
+}
+
+pi_status_t pi_permute_rows(const void *src, void *dst, const int32_t *perm, int64_t rows, int64_t row_bytes,
+                            int32_t *err, void *stream)
+{
+    if (rows < 0 || row_bytes < 0) return PI_ERR_INVALID_ARG;
+    if (rows == 0 || row_bytes == 0) return PI_OK;
+    const size_t n = (size_t)rows * (size_t)row_bytes;
+    int dev = 0;
+    pi_status_t s;
+    if ((s = cuda_status(cudaGetDevice(&dev)))) return s;
+    if ((s = check_ptr(src, n, 1, dev))) return s;
+    if ((s = check_ptr(dst, n, 1, dev))) return s;
+    if ((s = check_ptr(perm, (size_t)rows * 4, 4, dev))) return s;
+    if ((s = check_opt(err, 4, 4, dev))) return s;
+    const uintptr_t a = (uintptr_t)src, b = (uintptr_t)dst;
+    if (a < b + n && b < a + n) return PI_ERR_INVALID_ARG;
+    return cuda_status(launch_permute_rows(src, dst, perm, rows, row_bytes, err, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,121 @@
+// pi_common.cuh -- device helpers shared by the sm_103a kernels of libpi_ffn.so.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pi_internal.h"
+
+namespace pi {
+
+// element types and FFN kinds (numbering of include/pi_ffn.h)
+constexpr int DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2, DT_INT4 = 3;
+constexpr int KIND_GATED = 0, KIND_RELU = 1;
+
+// status codes written by kernels (pi_status_t values)
+constexpr uint32_t ST_DEVICE_CHECK = 6;
+constexpr uint32_t ST_TIMEOUT = 5;
+
+// Elements of a given type in one 16-byte chunk.
+template <int DT> struct Vec;
+template <> struct Vec<DT_F32>  { static constexpr int N = 4; };
+template <> struct Vec<DT_BF16> { static constexpr int N = 8; };
+template <> struct Vec<DT_F16>  { static constexpr int N = 8; };
+template <> struct Vec<DT_INT4> { static constexpr int N = 32; };
+
+// 16-byte load of weights that are streamed once per decode step: read-only
+// path, not kept in L1.
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_scale(const __half *p)
+{
+    unsigned short b;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(b) : "l"(p));
+    return __half2float(__ushort_as_half(b));
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue, and wait until the previous kernel's writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void set_status(uint32_t *status, uint32_t code)
+{
+    if (status) atomicCAS(status, 0u, code);
+}
+
+// Widen one 16-byte chunk of a 16/32-bit type to fp32.
+template <int DT>
+__device__ __forceinline__ void unpack(const uint4 &w, float (&o)[Vec<DT>::N]);
+
+template <>
+__device__ __forceinline__ void unpack<DT_F32>(const uint4 &w, float (&o)[4])
+{
+    o[0] = __uint_as_float(w.x);
+    o[1] = __uint_as_float(w.y);
+    o[2] = __uint_as_float(w.z);
+    o[3] = __uint_as_float(w.w);
+}
+
+template <>
+__device__ __forceinline__ void unpack<DT_BF16>(const uint4 &w, float (&o)[8])
+{
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = __uint_as_float(a[i] << 16);
+        o[2 * i + 1] = __uint_as_float(a[i] & 0xffff0000u);
+    }
+}
+
+template <>
+__device__ __forceinline__ void unpack<DT_F16>(const uint4 &w, float (&o)[8])
+{
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = *reinterpret_cast<const __half2 *>(&a[i]);
+        float2 f = __half22float2(h);
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
+}
+
+// Signed 4-bit value k (0..7) of a 32-bit word: bits [4k+3 : 4k], two's complement.
+__device__ __forceinline__ float nib(uint32_t w, int k)
+{
+    return (float)((int32_t)(w << (28 - 4 * k)) >> 28);
+}
+
+template <>
+__device__ __forceinline__ void unpack<DT_INT4>(const uint4 &w, float (&o)[32])
+{
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[8 * i + k] = nib(a[i], k);
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace pi

@@ -1,0 +1,107 @@
+// pi_internal.h -- launchers shared between the host side (pi_api.cu) and the kernel TUs.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <unordered_map>
+
+namespace pi {
+
+// Launch geometry shared by host and kernels.
+constexpr int NT = 256;               // threads per CTA of the CUDA-core kernels
+constexpr int NW = NT / 32;           // warps per CTA
+constexpr int PRED_ROWS_HIDDEN = 4;   // predictor hidden units per CTA (K1)
+constexpr int PRED_ROWS_LOGIT = 32;   // logits per CTA = one mask word (K2)
+constexpr int RED_COLS = 128;         // output columns per CTA of the partial-sum reduction
+constexpr int DOWN_GROUP_MIN = 16;    // smallest group of active neurons per fp32 partial
+constexpr int MAX_GROUPS = 256;       // at most this many partials per layer (group size grows with the count)
+constexpr size_t SMEM_VEC_CAP = 96 * 1024;  // shared memory for one staged batch tile of input vectors
+
+struct Launch {
+    dim3 grid, block;     // grid.x == 0: persistent grid, one wave of resident CTAs over nsm SMs
+    size_t smem;
+    cudaStream_t stream;
+    bool pdl;             // programmatic dependent launch after the previous kernel in the stream
+    int nsm;
+};
+
+// K1: hp[b,k] = max(0, (x_b * inv_rms_b) . p1_t[k])  for all k < r, b < B.
+cudaError_t launch_pred_hidden(const Launch &L, int pdt, int bt, const void *p1t, int d, int r,
+                               const float *x, const float *inv_rms, int B, float *hp);
+
+// K2: z = hp . p2_t[i] + b_pred[i]; mask bit i = OR_b (z > tau); the last CTA compacts
+// the mask words into ascending idx[] and *count. ticket must be 0 on entry (left 0).
+cudaError_t launch_pred_logits(const Launch &L, int pdt, int bt, const void *p2t, int r, int f,
+                               const float *b_pred, float tau, const float *hp, int B,
+                               uint32_t *maskw, uint32_t *ticket, int32_t *idx, int32_t *count);
+
+// K3: h[b,j] for the listed neurons j < *count.
+cudaError_t launch_ffn_h(const Launch &L, int wdt, int kind, int bt, const void *wg, const void *wu,
+                         const void *sg, const void *su, const float *bg, int d, int f,
+                         const float *x, const float *inv_rms, int B,
+                         const int32_t *idx, const int32_t *count, float *h, int ldh, uint32_t *status);
+
+// K4a: part[g,b,:] = sum_{j in group g} h[b,j] * w_down_t[idx[j],:]
+cudaError_t launch_ffn_down(const Launch &L, int wdt, int bt, const void *wd, const void *sd, int d, int f,
+                            const int32_t *idx, const int32_t *count, const float *h, int ldh, int B,
+                            float *part, uint32_t *status);
+
+// K4b: y = sum_g part[g] (fixed order). With xin: out = xin + y, and inv_rms of out
+// (last CTA) for the next layer. ticket must be 0 on entry (left 0).
+cudaError_t launch_reduce(const Launch &L, const float *part, int d, int B, int f, const int32_t *count,
+                          const float *xin, float *out, float *sumsq, uint32_t *ticket, float *inv_rms,
+                          float eps);
+
+// inv_rms[b] = 1 / sqrt(mean(x_b^2) + eps)
+cudaError_t launch_rms(const Launch &L, const float *x, int d, int B, float *inv_rms, float eps);
+
+// offline order
+cudaError_t launch_hot_first(const uint32_t *counts, int f, int32_t *perm, cudaStream_t s);
+cudaError_t launch_permute_rows(const void *src, void *dst, const int32_t *perm, int64_t rows, int64_t row_bytes,
+                                int32_t *err, cudaStream_t s);
+
+// groups of the down projection for a given active count (device and host agree)
+__host__ __device__ inline int down_group_size(int n)
+{
+    int g = (n + MAX_GROUPS - 1) / MAX_GROUPS;
+    return g < DOWN_GROUP_MIN ? DOWN_GROUP_MIN : g;
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_ex(const Launch &L, Kern kern, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = L.grid;
+    if (cfg.gridDim.x == 0) {
+        int occ = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, (int)(L.block.x * L.block.y),
+                                                                      L.smem);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim.x = (unsigned)(L.nsm * (occ > 0 ? occ : 1));
+    }
+    cfg.blockDim = L.block;
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = L.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Opt a kernel in to more than 48 KB of dynamic shared memory (remembered per kernel).
+template <typename Kern>
+cudaError_t ensure_smem(Kern kern, size_t bytes)
+{
+    static std::unordered_map<const void *, size_t> done;
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    auto it = done.find((const void *)kern);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done[(const void *)kern] = bytes;
+    return e;
+}
+
+}  // namespace pi

@@ -1,0 +1,444 @@
+"""Benchmark: activation-sparse FFN decode tokens/s and achieved HBM GB/s on GB300.
+
+One step = one decode token through every layer of the stack (pi_decode_stack:
+predictor -> union mask -> gate/up gather -> W_down axpy -> deterministic reduce,
+per layer). Default workload: ReluLLaMA-7B-shaped stack (32 gated-ReLU FFN layers,
+d=4096, f=11008, bf16, predictor rank 1024), batch 1, synthetic seeded weights and
+inputs. Each step streams ~1.9 GB of distinct weights, far more than the 126 MB
+L2, so steps run with inputs larger than L2 (no flush needed).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--batch B] [--no-cpu-baseline]
+
+--impl reference times the CPU fp64 oracle (the reference arm of this build) on the
+host cores, on a bounded sample of the same workload. Under torchrun (N > 1) every
+rank decodes its own token stream with the same weights (independent sequences,
+weak scaling, no data-path collective); only a barrier and a max over ranks of the
+timed region are exchanged.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workload import WORKLOADS, make_inputs, make_layer  # noqa: E402
+
+DEFAULT_WORKLOAD = "relullama7b_d4096_f11008_bf16_L32"
+METRIC = "sparse-FFN decode tokens/s (batch 1) and achieved HBM GB/s vs peak on GB300"
+POOL_TOKENS = 256
+WB = {"f32": 4.0, "bf16": 2.0, "f16": 2.0, "int4g128": 0.5}
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing (host-side logic; covered by gloo tests)
+# ------------------------------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def aggregate(ms_local: float, tokens_local: int, world: int):
+    """(max ms over ranks, total tokens over ranks): the whole job's timed region and work."""
+    if world == 1:
+        return ms_local, tokens_local
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+    n = torch.tensor([tokens_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------------
+# bytes
+# ------------------------------------------------------------------------------------------------
+
+def predictor_bytes(w) -> float:
+    """Dense predictor weights plus its fp32 bias, per layer."""
+    pb = WB[w.pdtype]
+    return w.r * w.d * pb + w.f * w.r * pb + w.f * 4
+
+
+def neuron_bytes(w) -> float:
+    """Bytes one active neuron costs: its gate(/up) and W_down rows, gate bias, int4 scales."""
+    rows = 3 if w.kind == "gated" else 2
+    b = rows * w.d * WB[w.wdtype] + 4
+    if w.wdtype == "int4g128":
+        b += rows * (w.d // 128) * 2
+    return b
+
+
+def step_bytes(w, counts_per_layer) -> float:
+    return float(sum(predictor_bytes(w) + c * neuron_bytes(w) for c in counts_per_layer))
+
+
+def kernel_bytes(w, kind: str, count: float, B: int) -> float:
+    """Algorithmic HBM bytes of one launch of a kernel kind (weights it must read once)."""
+    pb, wb = WB[w.pdtype], WB[w.wdtype]
+    sc = (w.d // 128) * 2 if w.wdtype == "int4g128" else 0
+    if kind == "pred_hidden":
+        return w.r * w.d * pb
+    if kind == "pred_logits":
+        return w.f * w.r * pb + w.f * 4
+    if kind == "ffn_h":
+        rows = 2 if w.kind == "gated" else 1
+        return count * (rows * (w.d * wb + sc) + 4)
+    if kind == "ffn_down":
+        return count * (w.d * wb + sc)
+    return 0.0
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:
+            self.proc.kill()
+        rows = [l for (ts, l) in self.lines if t0 - 0.05 <= ts <= t1 + 0.15]
+        if not rows:
+            rows = [l for (_, l) in self.lines[-3:]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            p = [x.strip() for x in r.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def build_model(w, device):
+    import activation_sparse_decode_pi_gb300 as P
+
+    layers = []
+    for l in range(w.n_layers):
+        L = make_layer(w, l, 0, device=device)
+        Lg, _ = P.apply_hot_first(L)
+        for k in ("p", "counts"):
+            Lg.pop(k, None)
+        layers.append(Lg)
+        del L
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return layers
+
+
+def cpu_baseline(w, B, seconds: float = 15.0, max_tokens: int = 64):
+    """The oracle, as it stands, on the host cores: tokens/s over a bounded sample."""
+    import oracle
+
+    x = make_inputs(w, POOL_TOKENS, B, 0, device="cpu").numpy()
+    layers = []
+    for l in range(w.n_layers):
+        L = make_layer(w, l, 0, device="cuda")
+        perm = oracle.hot_first_order(L["counts"].cpu().numpy())
+        Lo = oracle.layer_numpy(L)
+        for k in ("w_gate", "w_up", "w_down_t", "s_gate", "s_up", "s_down", "b_gate", "p2_t", "b_pred"):
+            if Lo.get(k) is not None:
+                Lo[k] = np.ascontiguousarray(Lo[k][perm])
+        layers.append(Lo)
+        del L
+    torch.cuda.empty_cache()
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_tokens and (time.perf_counter() - t0) < seconds:
+        oracle.stack(x[n].astype(np.float64), layers, w.kind, w.wdtype, w.pdtype)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n * B / dt, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{n} decode steps x batch {B} through all {w.n_layers} layers of {w.name} "
+                      f"(fp64 C oracle, OpenMP), {dt:.1f} s"}
+
+
+def run_ours(args):
+    import activation_sparse_decode_pi_gb300 as P
+
+    rank, local, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    B = args.batch
+    layers = build_model(w, dev)
+    ffn = P.SparseFFN.from_workload(w, layers, max_batch=B)
+    X = make_inputs(w, POOL_TOKENS, B, seed=1000 + rank, device=dev).contiguous()
+    x_in = torch.empty((B, w.d), dtype=torch.float32, device=dev)
+    x_out = torch.empty((B, w.d), dtype=torch.float32, device=dev)
+    counts = torch.zeros(w.n_layers, dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        # the next token's input arrives in the fixed input buffer, then one decode step
+        with torch.cuda.stream(s):
+            x_in.copy_(X[i % POOL_TOKENS], non_blocking=True)
+        P.pi_decode_stack(ffn.h, x_in, B, x_out, counts, None, s)
+
+    # ---- device-resident timing
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    e0.record(s)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    clocks = clk.stop(t0, t1)
+    barrier(world)
+    ms_local = e0.elapsed_time(e1)
+    ms, tokens = aggregate(ms_local, args.steps * B, world)
+    status = ffn.status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+
+    # ---- bytes actually touched: replay the same tokens (deterministic) collecting counts
+    per_step = []
+    cts = np.zeros((0, w.n_layers))
+    for i in range(args.steps if args.steps <= POOL_TOKENS else POOL_TOKENS):
+        step(args.warmup + i)
+        per_step.append(counts.clone())
+    if per_step:
+        cts = torch.stack(per_step).cpu().numpy().astype(np.float64)
+    mean_counts = cts.mean(axis=0) if len(cts) else np.zeros(w.n_layers)
+    bytes_per_step = step_bytes(w, mean_counts)
+    hbm_gbs = bytes_per_step * args.steps / (ms_local / 1e3) / 1e9
+
+    # ---- per-kernel durations (events around each launch, no overlap) for the roofline
+    prof_steps = min(16, POOL_TOKENS)
+    P.pi_profile_begin(ffn.h)
+    for i in range(prof_steps):
+        step(i)
+    prof = P.pi_profile_end(ffn.h)
+    peak, peak_src = load_peaks()
+    kinds = {k: v for k, v in prof.items() if v[1] > 0}
+    dom = max(kinds, key=lambda k: kinds[k][0])
+    dom_ms, dom_n = kinds[dom]
+    mean_count = float(mean_counts.mean()) if len(mean_counts) else 0.0
+    dom_bytes = kernel_bytes(w, dom, mean_count, B)
+    achieved = dom_bytes / (dom_ms / dom_n / 1e3) / 1e9
+    kernel_table = {k: {"ms_per_launch": v[0] / v[1], "launches": v[1],
+                        "share": v[0] / sum(x[0] for x in kinds.values()),
+                        "gbs": kernel_bytes(w, k, mean_count, B) / (v[0] / v[1] / 1e3) / 1e9}
+                    for k, v in kinds.items()}
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    Xh = X.cpu().pin_memory()
+    out_h = torch.empty((B, w.d), dtype=torch.float32).pin_memory()
+    e2e_steps = args.steps
+
+    def e2e_step(i):
+        with torch.cuda.stream(s):
+            x_in.copy_(Xh[i % POOL_TOKENS], non_blocking=True)
+            P.pi_decode_stack(ffn.h, x_in, B, x_out, counts, None, s)
+            out_h.copy_(x_out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(s)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    e2e_ms, e2e_tokens = aggregate(e0.elapsed_time(e1), e2e_steps * B, world)
+    barrier(world)
+
+    launches_per_step = 1 + 5 * w.n_layers
+    line = {
+        "metric": METRIC,
+        "value": tokens / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.wdtype,
+        "data": "synthetic (seeded weights with the workload's shapes and Zipf activation statistics; x ~ N(0,1))",
+        "config": {"workload": w.name, "d": w.d, "f": w.f, "r": w.r, "layers": w.n_layers, "kind": w.kind,
+                   "weights": w.wdtype, "predictor": w.pdtype, "batch": B, "global_batch": B * world,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {bytes_per_step / 1e9:.2f} GB of distinct weights per step"},
+        "hbm_gbs": hbm_gbs,
+        "hbm_frac": hbm_gbs / peak,
+        "bytes_per_step": bytes_per_step,
+        "mean_active_per_layer": mean_count,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s"},
+        "kernels": kernel_table,
+        "clocks": clocks,
+        "e2e": {"value": e2e_tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": B * w.d * 4,
+                "d2h_bytes_per_step": B * w.d * 4},
+        "gpu_launches": args.steps * launches_per_step,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del layers, ffn
+        torch.cuda.empty_cache()
+        line["cpu_baseline"] = cpu_baseline(w, B)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ------------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    w = WORKLOADS[args.workload]
+    B = args.batch
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = make_inputs(w, POOL_TOKENS, B, 1000, device="cpu").numpy()
+    layers = []
+    for l in range(w.n_layers):
+        L = make_layer(w, l, 0, device=gen_dev)
+        perm = oracle.hot_first_order(L["counts"].cpu().numpy())
+        Lo = oracle.layer_numpy(L)
+        for k in ("w_gate", "w_up", "w_down_t", "s_gate", "s_up", "s_down", "b_gate", "p2_t", "b_pred"):
+            if Lo.get(k) is not None:
+                Lo[k] = np.ascontiguousarray(Lo[k][perm])
+        layers.append(Lo)
+    for i in range(args.warmup):
+        oracle.stack(x[i % POOL_TOKENS].astype(np.float64), layers, w.kind, w.wdtype, w.pdtype)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.stack(x[(args.warmup + i) % POOL_TOKENS].astype(np.float64), layers, w.kind, w.wdtype, w.pdtype)
+    dt = time.perf_counter() - t0
+    v = args.steps * B / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded workload as the GPU arm)",
+        "config": {"workload": w.name, "d": w.d, "f": w.f, "r": w.r, "layers": w.n_layers, "batch": B},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"{args.steps} timed decode steps x batch {B} (after {args.warmup} warm-up) "
+                                   f"through all {w.n_layers} layers"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        args.steps = 3 if args.steps is None else args.steps
+        args.warmup = 1 if args.warmup is None else args.warmup
+        run_reference(args)
+    else:
+        args.steps = 2000 if args.steps is None else args.steps
+        args.warmup = 20 if args.warmup is None else max(3, args.warmup)
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

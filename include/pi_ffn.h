@@ -1,0 +1,200 @@
+/*
+ * pi_ffn.h -- C ABI of libpi_ffn.so: activation-sparse FFN decode on one GB300 (sm_103a).
+ *
+ * The method is the one the PowerInfer pages describe: per layer, a small
+ * predictor decides which FFN neurons will be non-zero, and only those neurons'
+ * weight rows are read ("PowerInfer" paper walk-through page, section
+ * "inference flow": input reaches a layer -> predictor -> compute the predicted
+ * neurons -> merge -> next layer; summary page, Methodology: neuron-aware sparse
+ * operators that do matrix-vector products at neuron granularity).
+ * Here the whole model is resident in HBM; nothing runs on the CPU at inference.
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers (cudaMalloc'd or managed), borrowed:
+ *    the caller owns them and keeps them alive while the library may read them.
+ *    Host pointers are rejected with PI_ERR_INVALID_ARG before any launch.
+ *  - Matrices are row-major. Every FFN matrix is stored neuron-major: row i of
+ *    w_gate / w_up / w_down_t holds the d weights of neuron i (w_down_t is the
+ *    transpose of the down projection). Neurons are expected in hot-first order
+ *    (pi_hot_first_order), which keeps frequently active rows contiguous.
+ *  - Element types: PI_F32 (fp32), PI_BF16, PI_F16, PI_INT4_G128. INT4_G128:
+ *    per-row groups of 128 consecutive elements share one fp16 scale s; the
+ *    value is q*s with q a signed 4-bit two's-complement integer; element 2k is
+ *    the low nibble of byte k. Scales are [rows x d/128] fp16.
+ *  - Activations and outputs are fp32; every dot product accumulates in fp32.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). All calls after
+ *    pi_ffn_create are asynchronous on `stream`; they validate arguments on the
+ *    host first and return an error without launching anything if one is bad.
+ *  - Errors found by the kernels (an active index outside [0, f), a count
+ *    outside [0, f]) are recorded in a device status word and the offending
+ *    entry is skipped; pi_get_status() reports them. No kernel traps.
+ *  - No C++ exception crosses this boundary. Not thread-safe per handle.
+ */
+#ifndef PI_FFN_H
+#define PI_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PI_FFN_ABI_VERSION 1
+
+typedef enum {
+    PI_OK = 0,
+    PI_ERR_INVALID_ARG = 1,   /* bad size, NULL / misaligned / host pointer, layer or batch out of range */
+    PI_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement (e.g. int4 with d % 128 != 0) */
+    PI_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+    PI_ERR_OOM = 4,           /* workspace allocation failed */
+    PI_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up */
+    PI_ERR_DEVICE_CHECK = 6   /* a kernel rejected an input entry (see conventions) */
+} pi_status_t;
+
+typedef enum {
+    PI_FFN_GATED_RELU = 0,    /* LLaMA-style: h_i = ReLU(u.Wg_i + bg_i) * (u.Wu_i) */
+    PI_FFN_RELU = 1           /* OPT/Falcon-style: h_i = ReLU(u.W1_i + b1_i); w_gate holds W1 */
+} pi_ffn_kind_t;
+
+typedef enum { PI_F32 = 0, PI_BF16 = 1, PI_F16 = 2, PI_INT4_G128 = 3 } pi_dtype_t;
+
+/* Shape and numerics of a layer stack. All layers share it. */
+typedef struct {
+    int32_t d;          /* model width; multiple of 8 (of 128 for PI_INT4_G128) */
+    int32_t f;          /* FFN width (neurons), >= 1 */
+    int32_t r;          /* predictor rank, multiple of 8 */
+    int32_t n_layers;   /* >= 1 */
+    int32_t max_batch;  /* largest B any call will pass, 1..256; sizes the workspace */
+    int32_t kind;       /* pi_ffn_kind_t */
+    int32_t wdtype;     /* pi_dtype_t of w_gate / w_up / w_down_t */
+    int32_t pdtype;     /* pi_dtype_t of p1_t / p2_t: PI_F32, PI_BF16 or PI_F16 */
+    float tau_logit;    /* threshold on the predictor logit; neuron active iff z > tau (0 <=> sigmoid > 0.5) */
+} pi_ffn_desc_t;
+
+/* One layer's weights (device pointers, borrowed; 16-byte aligned). */
+typedef struct {
+    const void *w_gate;    /* [f x d] Wg (gated) or W1 (non-gated) */
+    const void *w_up;      /* [f x d] Wu; NULL for PI_FFN_RELU */
+    const void *w_down_t;  /* [f x d] W_down transposed */
+    const void *s_gate;    /* int4 only: fp16 [f x d/128]; else NULL */
+    const void *s_up;      /* int4 + gated only; else NULL */
+    const void *s_down;    /* int4 only; else NULL */
+    const float *b_gate;   /* [f] fp32 gate / fc1 bias, or NULL (zero) */
+    const void *p1_t;      /* [r x d] predictor first layer, transposed (row k = weights of hidden unit k) */
+    const void *p2_t;      /* [f x r] predictor second layer, transposed (row i = weights of neuron i's logit) */
+    const float *b_pred;   /* [f] fp32 predictor bias, or NULL (zero) */
+} pi_layer_weights_t;
+
+typedef struct pi_ffn pi_ffn_t;
+
+/*
+ * Create a handle for a stack of desc->n_layers layers. `layers` (host array of
+ * n_layers descriptors) is copied; the weight memory it points to is borrowed.
+ * Allocates the workspace (predictor hidden state, mask words, active indices,
+ * h, fp32 partial sums, stack buffers, status word) on the current device.
+ * Returns PI_ERR_INVALID_ARG / PI_ERR_UNSUPPORTED / PI_ERR_OOM / PI_ERR_CUDA with
+ * *out = NULL on failure.
+ */
+pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_layer_weights_t *layers);
+
+/* Free the workspace and the handle (waits for the device first). NULL is a no-op. */
+void pi_ffn_destroy(pi_ffn_t *h);
+
+/*
+ * Activation predictor of layer `layer` ("PowerInfer" walk-through page, section
+ * "activation predictor", eq. a = sigmoid(x Wp + b_p), neuron i active when
+ * a_i > tau; read as a two-layer low-rank MLP):
+ *   hp[b,k] = max(0, u[b,:] . p1_t[k,:])               k < r
+ *   z[b,i]  = hp[b,:] . p2_t[i,:] + b_pred[i]          i < f
+ *   neuron i is active iff z[b,i] > tau_logit for at least one row b (union over the batch).
+ * u:     [B x d] fp32 device, the layer input (already normalised).
+ * idx:   [f] int32 device, out: the active neurons in ascending order (entries >= *count unspecified).
+ * count: one int32 device, out: number of active neurons.
+ * 1 <= B <= max_batch.
+ */
+pi_status_t pi_predict(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
+                       int32_t *idx, int32_t *count, void *stream);
+
+/*
+ * Neuron-sparse FFN of layer `layer` over a given active list (same page, section
+ * "technical details", eq. FFN(x) = sigma(x W1) (.) (x W2) W3, sigma = ReLU), reading
+ * only the listed neurons' rows:
+ *   gated:     h[b,j] = max(0, u_b . Wg_i + bg_i) * (u_b . Wu_i),    i = idx[j], j < *count
+ *   non-gated: h[b,j] = max(0, u_b . W1_i + b1_i)
+ *   y[b,:]     = sum_j h[b,j] * w_down_t[i,:]
+ * The sum is deterministic: fixed groups of consecutive list entries are summed in
+ * list order into fp32 partials, and the partials are added in a fixed order, so the
+ * bits of y depend only on the inputs. Any index list is accepted (ascending or not,
+ * empty when *count == 0); entries outside [0, f) are skipped and flagged.
+ * u: [B x d] fp32; idx: [>= *count] int32; count: one int32 (device); y: [B x d] fp32 out.
+ */
+pi_status_t pi_sparse_ffn(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
+                          const int32_t *idx, const int32_t *count, float *y, void *stream);
+
+/*
+ * One decode step through all n_layers layers (the walk-through page's per-layer
+ * inference flow, merge -> next layer), with a parameter-free pre-norm residual
+ * between layers (the pages are silent about non-FFN layers):
+ *   x_0 = x0;  u_l = x_l / sqrt(mean(x_l^2) + 1e-6);  x_{l+1} = x_l + FFN_l(u_l over predict_l(u_l))
+ * x0: [B x d] fp32 device; x_out: [B x d] fp32 device, out (= x_L).
+ * counts: [n_layers] int32 device out (active count per layer), or NULL.
+ * idx_out: [n_layers x f] int32 device out (layer l's ascending active list in row l), or NULL.
+ * No host synchronisation inside. Outside stream capture the step is recorded once
+ * into a CUDA graph per (B, pointer set) and replayed.
+ */
+pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_out,
+                            int32_t *counts, int32_t *idx_out, void *stream);
+
+/*
+ * Offline hot-first order (walk-through page, section "offline profiling", code
+ * block: per-neuron activation counts sorted in descending order). perm[k] = the
+ * neuron that moves to position k: counts descending, equal counts keep their
+ * original (ascending) order. counts: [f] uint32 device; perm: [f] int32 device out.
+ */
+pi_status_t pi_hot_first_order(const uint32_t *counts, int32_t f, int32_t *perm, void *stream);
+
+/*
+ * Apply an order to a row-major matrix: row k of dst = row perm[k] of src.
+ * rows rows of row_bytes bytes each; src and dst must not overlap.
+ * err: one int32 device counter (or NULL), incremented per perm entry outside
+ * [0, rows); such destination rows are left unwritten.
+ */
+pi_status_t pi_permute_rows(const void *src, void *dst, const int32_t *perm, int64_t rows,
+                            int64_t row_bytes, int32_t *err, void *stream);
+
+/*
+ * Per-kernel timing (tracing aid). Between pi_profile_begin and pi_profile_end, every
+ * kernel the handle launches is bracketed by two CUDA events on its stream, and
+ * pi_decode_stack runs without its CUDA graph and without programmatic overlap, so
+ * each bracket is that kernel's own duration. pi_profile_end waits for the device and
+ * writes, per kernel kind k < n_kinds (pi_kernel_kind_t), the summed milliseconds
+ * ms[k] and the number of launches launches[k] (either array may be NULL).
+ */
+typedef enum {
+    PI_K_RMS = 0,          /* RMS scale of the stack input */
+    PI_K_PRED_HIDDEN = 1,  /* predictor hidden layer */
+    PI_K_PRED_LOGITS = 2,  /* predictor logits, union mask, compaction */
+    PI_K_FFN_H = 3,        /* gate/up gather-GEMV */
+    PI_K_FFN_DOWN = 4,     /* row-sparse W_down axpy into fp32 partials */
+    PI_K_REDUCE = 5,       /* deterministic reduction (+ residual, next RMS scale) */
+    PI_K_COUNT = 6
+} pi_kernel_kind_t;
+
+pi_status_t pi_profile_begin(pi_ffn_t *h);
+pi_status_t pi_profile_end(pi_ffn_t *h, float *ms, int32_t *launches, int32_t n_kinds);
+
+/* Wait for all work on the device, return the first kernel-recorded error and clear it. */
+pi_status_t pi_get_status(pi_ffn_t *h);
+
+/* Static text for a status code. */
+const char *pi_status_string(pi_status_t s);
+
+/* PI_FFN_ABI_VERSION of the loaded library. */
+int32_t pi_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PI_FFN_H */

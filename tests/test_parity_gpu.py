@@ -1,0 +1,255 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bars: index work (hot-first order, row permutation, active lists) bit-exact,
+except active-set membership of neurons whose oracle logit lies within 1e-4 of
+the threshold; FFN outputs within relative L2 1e-3 (fp32/bf16/fp16 weights) or
+5e-3 (int4) of the oracle evaluated on the same active list.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_cases import TOL, band_mask, build_layers, rel_l2, rms_inputs, to_dev
+from workload import WORKLOADS, make_inputs, scaled
+
+pytestmark = pytest.mark.gpu
+W = list(WORKLOADS.values())
+SMALL = dict(d=640, f=1007, r=72)          # several K2 words + a ragged word, several K3/K4a tiles
+MID = dict(d=2304, f=3001, r=136)
+
+
+@pytest.fixture(scope="module")
+def P():
+    import activation_sparse_decode_pi_gb300 as P
+
+    return P
+
+
+def _wl(wi, shape, n_layers=1):
+    return scaled(W[wi], n_layers=n_layers, **shape)
+
+
+# ------------------------------------------------------------------ offline order --------------
+
+@pytest.mark.parametrize("f", [1, 31, 1000, 4099, 49152])
+def test_hot_first_order(P, f):
+    rng = np.random.default_rng(f)
+    for counts in (rng.integers(0, 20, f), np.zeros(f, np.int64), np.arange(f)[::-1].copy(),
+                   rng.integers(0, 2**31 - 1, f)):
+        perm = P.hot_first_order(to_dev(counts.astype(np.int32)))
+        assert np.array_equal(perm.cpu().numpy(), oracle.hot_first_order(counts))
+
+
+@pytest.mark.parametrize("row_bytes", [16, 6, 100, 2048])
+def test_permute_rows(P, row_bytes):
+    rng = np.random.default_rng(row_bytes)
+    rows = 777
+    src = rng.integers(0, 256, (rows, row_bytes), dtype=np.uint8)
+    perm = rng.permutation(rows).astype(np.int32)
+    dst = P.permute_rows(to_dev(src), to_dev(perm))
+    assert np.array_equal(dst.cpu().numpy(), src[perm])
+    # out-of-range entries are counted and their rows left unwritten
+    bad = perm.copy()
+    bad[[3, 50]] = [-1, rows]
+    out = torch.zeros((rows, row_bytes), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    P.pi_permute_rows(to_dev(src), out, to_dev(bad), rows, row_bytes, err)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert int(err.item()) == 2
+    assert np.all(o[[3, 50]] == 0)
+    keep = np.setdiff1d(np.arange(rows), [3, 50])
+    assert np.array_equal(o[keep], src[bad[keep]])
+
+
+# ------------------------------------------------------------------ predictor -----------------
+
+@pytest.mark.parametrize("B", [1, 3, 8, 16])
+@pytest.mark.parametrize("wi", range(5))
+def test_predict_small(P, wi, B):
+    w = _wl(wi, SMALL)
+    (Lg, Lo), = build_layers(w, [0])
+    ffn = P.SparseFFN.from_workload(w, [Lg], max_batch=B)
+    u = rms_inputs(w, B)[0]
+    idx, cnt = ffn.predict(0, to_dev(u))
+    torch.cuda.synchronize()
+    n = int(cnt.item())
+    gi = idx[:n].cpu().numpy()
+    pr = oracle.predict(u.astype(np.float64), Lo["p1_t"], Lo["p2_t"], Lo["b_pred"], w.pdtype)
+    assert 0 < pr["count"] < w.f
+    assert np.all(np.diff(gi) > 0), "active list must be ascending and unique"
+    diff = np.setxor1d(gi, pr["idx"])
+    assert np.all(band_mask(pr["z"])[diff]), f"{diff.size} out-of-band mismatches"
+    assert ffn.status() == 0
+    ffn.close()
+
+
+# ------------------------------------------------------------------ sparse FFN ----------------
+
+def _lists(rng, f, pred_idx):
+    sub = rng.choice(f, size=min(f, 97), replace=False).astype(np.int32)   # unsorted on purpose
+    return {"predicted": pred_idx.astype(np.int32), "all": np.arange(f, dtype=np.int32),
+            "empty": np.zeros(0, np.int32), "random_unsorted": sub, "single": np.array([f - 1], np.int32)}
+
+
+@pytest.mark.parametrize("B", [1, 4, 16])
+@pytest.mark.parametrize("wi", range(5))
+def test_sparse_ffn_small(P, wi, B):
+    w = _wl(wi, SMALL)
+    (Lg, Lo), = build_layers(w, [0])
+    ffn = P.SparseFFN.from_workload(w, [Lg], max_batch=B)
+    u = rms_inputs(w, B)[0]
+    u64 = u.astype(np.float64)
+    pr = oracle.predict(u64, Lo["p1_t"], Lo["p2_t"], Lo["b_pred"], w.pdtype)
+    rng = np.random.default_rng(wi * 10 + B)
+    ud = to_dev(u)
+    for name, lst in _lists(rng, w.f, pr["idx"]).items():
+        idx = torch.zeros(max(1, lst.size), dtype=torch.int32, device="cuda")
+        idx[: lst.size] = to_dev(lst) if lst.size else idx[:0]
+        cnt = torch.tensor([lst.size], dtype=torch.int32, device="cuda")
+        y = ffn.sparse_ffn(0, ud, idx, cnt)
+        torch.cuda.synchronize()
+        _, yo = oracle.sparse_ffn(u64, Lo, lst, w.kind, w.wdtype)
+        yg = y.cpu().numpy()
+        if lst.size == 0:
+            assert np.all(yg == 0.0)
+        else:
+            err = rel_l2(yg, yo)
+            assert err <= TOL[w.wdtype], (name, err)
+    assert ffn.status() == 0
+    ffn.close()
+
+
+def test_sparse_ffn_is_deterministic(P):
+    w = _wl(1, MID)
+    (Lg, Lo), = build_layers(w, [0])
+    ffn = P.SparseFFN.from_workload(w, [Lg], max_batch=4)
+    ud = to_dev(rms_inputs(w, 4)[0])
+    idx = torch.arange(w.f, dtype=torch.int32, device="cuda")
+    cnt = torch.tensor([w.f], dtype=torch.int32, device="cuda")
+    y1 = ffn.sparse_ffn(0, ud, idx, cnt).clone()
+    y2 = ffn.sparse_ffn(0, ud, idx, cnt)
+    assert torch.equal(y1, y2)
+    ffn.close()
+
+
+def test_device_checks(P):
+    """Out-of-range list entries and counts are flagged, skipped, and never read."""
+    w = _wl(0, SMALL)
+    (Lg, Lo), = build_layers(w, [0])
+    ffn = P.SparseFFN.from_workload(w, [Lg], max_batch=2)
+    u = rms_inputs(w, 2)[0]
+    lst = np.array([5, w.f + 7, 9, -3, 100], np.int32)
+    y = ffn.sparse_ffn(0, to_dev(u), to_dev(lst), torch.tensor([5], dtype=torch.int32, device="cuda"))
+    assert ffn.status() == P.PI_ERR_DEVICE_CHECK
+    assert ffn.status() == 0   # cleared
+    _, yo = oracle.sparse_ffn(u.astype(np.float64), Lo, [5, 9, 100], w.kind, w.wdtype)
+    assert rel_l2(y.cpu().numpy(), yo) <= TOL[w.wdtype]
+    # a count above f is clamped to f
+    idx = torch.arange(w.f, dtype=torch.int32, device="cuda")
+    y = ffn.sparse_ffn(0, to_dev(u), idx, torch.tensor([w.f + 50], dtype=torch.int32, device="cuda"))
+    assert ffn.status() == P.PI_ERR_DEVICE_CHECK
+    yd = oracle.dense_ffn(u.astype(np.float64), Lo, w.kind, w.wdtype)
+    assert rel_l2(y.cpu().numpy(), yd) <= TOL[w.wdtype]
+    ffn.close()
+
+
+def test_host_side_rejections(P):
+    w = _wl(1, SMALL)
+    (Lg, Lo), = build_layers(w, [0])
+    ffn = P.SparseFFN.from_workload(w, [Lg], max_batch=2)
+    u = to_dev(rms_inputs(w, 2)[0])
+    idx = torch.zeros(w.f, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    host = np.zeros((2, w.d), np.float32)
+    with pytest.raises(P.PiError) as e:
+        P.pi_predict(ffn.h, 0, host.ctypes.data, 2, idx, cnt)      # host pointer
+    assert e.value.code == P.PI_ERR_INVALID_ARG
+    with pytest.raises(P.PiError):
+        P.pi_predict(ffn.h, 0, u.data_ptr() + 4, 1, idx, cnt)     # misaligned
+    with pytest.raises(P.PiError):
+        P.pi_predict(ffn.h, 0, u, 3, idx, cnt)                    # B > max_batch
+    with pytest.raises(P.PiError):
+        P.pi_predict(ffn.h, 1, u, 2, idx, cnt)                    # layer out of range
+    with pytest.raises(P.PiError):
+        P.pi_sparse_ffn(ffn.h, 0, u, 2, idx, cnt, None)           # NULL output
+    # a layer whose weights would run past the end of their allocation
+    big = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    seg = [s for s in torch.cuda.memory_snapshot()
+           if s["address"] <= big.data_ptr() < s["address"] + s["total_size"]][0]
+    end = seg["address"] + seg["total_size"]
+    bad = dict(Lg)
+    bad["w_gate"] = end - 4096
+    with pytest.raises(P.PiError) as e:
+        P.SparseFFN.from_workload(w, [bad])
+    assert e.value.code == P.PI_ERR_INVALID_ARG
+    ffn.close()
+
+
+# ------------------------------------------------------------------ layer stack ---------------
+
+def _stack_check(P, w, B, tokens, seed=0):
+    layers = build_layers(w, range(w.n_layers), seed)
+    ffn = P.SparseFFN.from_workload(w, [g for g, _ in layers], max_batch=B)
+    X = make_inputs(w, tokens, B, seed, device="cpu").numpy()
+    compared, flips = 0, 0
+    for t in range(tokens):
+        x0 = to_dev(X[t])
+        counts = torch.zeros(w.n_layers, dtype=torch.int32, device="cuda")
+        idx_out = torch.zeros((w.n_layers, w.f), dtype=torch.int32, device="cuda")
+        xo = ffn.decode_stack(x0, counts=counts, idx_out=idx_out)
+        xo2 = ffn.decode_stack(x0, counts=counts, idx_out=idx_out).clone()   # graph replay
+        torch.cuda.synchronize()
+        assert torch.equal(xo, xo2), "decode step is not deterministic"
+        st = oracle.stack(X[t].astype(np.float64), [o for _, o in layers], w.kind, w.wdtype, w.pdtype)
+        cg = counts.cpu().numpy()
+        ig = idx_out.cpu().numpy()
+        same = True
+        for l in range(w.n_layers):
+            gi = ig[l, : cg[l]]
+            assert np.all(np.diff(gi) > 0)
+            diff = np.setxor1d(gi, st["idx"][l])
+            if diff.size:
+                # allowed only inside the band, and then later layers no longer compare
+                assert np.all(st["zmin"][l][diff] < oracle.BAND), (l, diff)
+                same = False
+                flips += 1
+                break
+        if same:
+            compared += 1
+            err = rel_l2(xo.cpu().numpy() - X[t], st["x_out"] - X[t])
+            assert err <= TOL[w.wdtype], err
+    assert ffn.status() == 0
+    ffn.close()
+    return compared, flips
+
+
+@pytest.mark.parametrize("wi", range(5))
+def test_decode_stack_small(P, wi):
+    w = _wl(wi, SMALL, n_layers=3)
+    for B in sorted({1, max(W[wi].batches)}):
+        compared, flips = _stack_check(P, w, B, tokens=2)
+        assert compared >= 1
+
+
+def test_decode_stack_under_user_capture(P):
+    """Inside a caller's stream capture the step is enqueued into the caller's graph."""
+    w = _wl(2, SMALL, n_layers=2)
+    layers = build_layers(w, range(2))
+    ffn = P.SparseFFN.from_workload(w, [g for g, _ in layers], max_batch=4)
+    x0 = to_dev(make_inputs(w, 1, 4).numpy()[0])
+    ref = ffn.decode_stack(x0).clone()
+    out = torch.empty_like(x0)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        ffn.decode_stack(x0, x_out=out, stream=s)      # warm-up outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            ffn.decode_stack(x0, x_out=out, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    ffn.close()
