@@ -34,8 +34,9 @@ KINDS = {"gated": PI_FFN_GATED_RELU, "relu": PI_FFN_RELU}
 EXPORTS = (
     "pi_ffn_create", "pi_ffn_destroy", "pi_predict", "pi_sparse_ffn", "pi_decode_stack",
     "pi_hot_first_order", "pi_permute_rows", "pi_get_status", "pi_status_string", "pi_abi_version",
-    "pi_profile_begin", "pi_profile_end",
+    "pi_profile_begin", "pi_profile_end", "pi_sparse_ffn_noalloc",
 )
+PI_NOALLOC_SCRATCH_BYTES = 16 << 20
 KERNEL_KINDS = ("rms", "pred_hidden", "pred_logits", "ffn_h", "ffn_down", "reduce")
 
 
@@ -75,6 +76,9 @@ _lib.pi_status_string.restype = ctypes.c_char_p
 _lib.pi_status_string.argtypes = [ctypes.c_int]
 _lib.pi_abi_version.restype = _I32
 _lib.pi_abi_version.argtypes = []
+_lib.pi_sparse_ffn_noalloc.restype = ctypes.c_int
+_lib.pi_sparse_ffn_noalloc.argtypes = [ctypes.POINTER(PiFfnDesc), ctypes.POINTER(PiLayerWeights), _P, _I32, _P, _P,
+                                       _P, _P, _P]
 _lib.pi_profile_begin.restype = ctypes.c_int
 _lib.pi_profile_begin.argtypes = [_P]
 _lib.pi_profile_end.restype = ctypes.c_int
@@ -142,6 +146,12 @@ def pi_sparse_ffn(h, layer, u, B, idx, count, y, stream=None) -> None:
 def pi_decode_stack(h, x0, B, x_out, counts=None, idx_out=None, stream=None) -> None:
     _check(_lib.pi_decode_stack(h, _ptr(x0), B, _ptr(x_out), _ptr(counts), _ptr(idx_out), _stream(stream)),
            "pi_decode_stack")
+
+
+def pi_sparse_ffn_noalloc(desc, layer, u, B, idx, count, y, status=None, stream=None) -> None:
+    """pi_sparse_ffn without a handle and without any device allocation (static library scratch)."""
+    _check(_lib.pi_sparse_ffn_noalloc(ctypes.byref(desc), ctypes.byref(layer), _ptr(u), B, _ptr(idx), _ptr(count),
+                                      _ptr(y), _ptr(status), _stream(stream)), "pi_sparse_ffn_noalloc")
 
 
 def pi_hot_first_order(counts, f, perm, stream=None) -> None:

@@ -91,12 +91,13 @@ cudaError_t launch_ex(const Launch &L, Kern kern, Args... args)
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Opt a kernel in to more than 48 KB of dynamic shared memory (remembered per kernel).
+// Opt a kernel in to its dynamic shared memory when dynamic + static shared memory
+// could pass the default 48 KB limit (remembered per kernel).
 template <typename Kern>
 cudaError_t ensure_smem(Kern kern, size_t bytes)
 {
     static std::unordered_map<const void *, size_t> done;
-    if (bytes <= 48 * 1024) return cudaSuccess;
+    if (bytes + 8 * 1024 <= 48 * 1024) return cudaSuccess;
     auto it = done.find((const void *)kern);
     if (it != done.end() && it->second >= bytes) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);

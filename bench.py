@@ -228,6 +228,15 @@ def cpu_baseline(w, B, seconds: float = 15.0, max_tokens: int = 64):
                       f"(fp64 C oracle, OpenMP), {dt:.1f} s"}
 
 
+def workload_of(args):
+    import dataclasses
+
+    w = WORKLOADS[args.workload]
+    if args.layers:
+        w = dataclasses.replace(w, n_layers=min(args.layers, w.n_layers))
+    return w
+
+
 def run_ours(args):
     import activation_sparse_decode_pi_gb300 as P
 
@@ -238,7 +247,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     B = args.batch
     layers = build_model(w, dev)
     ffn = P.SparseFFN.from_workload(w, layers, max_batch=B)
@@ -386,7 +395,7 @@ def run_reference(args):
         return
     import oracle
 
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     B = args.batch
     gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
     x = make_inputs(w, POOL_TOKENS, B, 1000, device="cpu").numpy()
@@ -428,6 +437,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="use only the first L layers (small-footprint profiling runs; default: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.impl == "reference":

@@ -184,6 +184,33 @@ typedef enum {
 pi_status_t pi_profile_begin(pi_ffn_t *h);
 pi_status_t pi_profile_end(pi_ffn_t *h, float *ms, int32_t *launches, int32_t n_kinds);
 
+/*
+ * Allocation-free variant of pi_sparse_ffn for callers that cannot call cudaMalloc
+ * (code inside an allocator callback, a plugin whose host owns all device memory,
+ * a runtime that forbids allocation after start-up), and so cannot create a handle.
+ * The pages have no counterpart: this is a deployment convenience, not a step of
+ * the method.
+ *
+ * Computes exactly what pi_sparse_ffn computes for one layer described by `desc`
+ * (only d, f, r, kind, wdtype are read) and `layer`, with the same kernels. Its
+ * scratch memory (h and the fp32 partial sums) is a static device array inside the
+ * library, PI_NOALLOC_SCRATCH_BYTES per GPU, held from the library's load on that GPU
+ * until process exit. The call needs (B*f rounded up to 64 + 256*B*d) * 4 bytes of it
+ * and returns PI_ERR_UNSUPPORTED, launching nothing, when that exceeds the array.
+ * Set-up: the first call on each device looks up the array's device address with
+ * that device current; make that first call before any stream capture.
+ * Every call shares the array and it keeps the previous call's contents (this path
+ * needs none of it zeroed); calls whose kernels overlap on the GPU race on it, so
+ * order them on one stream. status: optional int32 device word; a kernel that
+ * rejects a list entry or count sets it to PI_ERR_DEVICE_CHECK if it is 0 (clear it
+ * before the call). No cudaMalloc, cudaFree or other allocating call is made.
+ */
+#define PI_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+pi_status_t pi_sparse_ffn_noalloc(const pi_ffn_desc_t *desc, const pi_layer_weights_t *layer,
+                                  const float *u, int32_t B, const int32_t *idx, const int32_t *count,
+                                  float *y, int32_t *status, void *stream);
+
 /* Wait for all work on the device, return the first kernel-recorded error and clear it. */
 pi_status_t pi_get_status(pi_ffn_t *h);
 
