@@ -34,10 +34,10 @@ KINDS = {"gated": PI_FFN_GATED_RELU, "relu": PI_FFN_RELU}
 EXPORTS = (
     "pi_ffn_create", "pi_ffn_destroy", "pi_predict", "pi_sparse_ffn", "pi_decode_stack",
     "pi_hot_first_order", "pi_permute_rows", "pi_get_status", "pi_status_string", "pi_abi_version",
-    "pi_profile_begin", "pi_profile_end", "pi_sparse_ffn_noalloc",
+    "pi_profile_begin", "pi_profile_end", "pi_sparse_ffn_noalloc", "pi_selftest_grid_barrier",
 )
 PI_NOALLOC_SCRATCH_BYTES = 16 << 20
-KERNEL_KINDS = ("rms", "pred_hidden", "pred_logits", "ffn_h", "ffn_down", "reduce")
+KERNEL_KINDS = ("rms", "pred_hidden", "pred_logits", "ffn_h", "ffn_down", "reduce", "decode_stack")
 
 
 class PiFfnDesc(ctypes.Structure):
@@ -79,6 +79,8 @@ _lib.pi_abi_version.argtypes = []
 _lib.pi_sparse_ffn_noalloc.restype = ctypes.c_int
 _lib.pi_sparse_ffn_noalloc.argtypes = [ctypes.POINTER(PiFfnDesc), ctypes.POINTER(PiLayerWeights), _P, _I32, _P, _P,
                                        _P, _P, _P]
+_lib.pi_selftest_grid_barrier.restype = ctypes.c_int
+_lib.pi_selftest_grid_barrier.argtypes = [_P, _I32, _P]
 _lib.pi_profile_begin.restype = ctypes.c_int
 _lib.pi_profile_begin.argtypes = [_P]
 _lib.pi_profile_end.restype = ctypes.c_int
@@ -152,6 +154,10 @@ def pi_sparse_ffn_noalloc(desc, layer, u, B, idx, count, y, status=None, stream=
     """pi_sparse_ffn without a handle and without any device allocation (static library scratch)."""
     _check(_lib.pi_sparse_ffn_noalloc(ctypes.byref(desc), ctypes.byref(layer), _ptr(u), B, _ptr(idx), _ptr(count),
                                       _ptr(y), _ptr(status), _stream(stream)), "pi_sparse_ffn_noalloc")
+
+
+def pi_selftest_grid_barrier(work, extra, stream=None) -> None:
+    _check(_lib.pi_selftest_grid_barrier(_ptr(work), extra, _stream(stream)), "pi_selftest_grid_barrier")
 
 
 def pi_hot_first_order(counts, f, perm, stream=None) -> None:

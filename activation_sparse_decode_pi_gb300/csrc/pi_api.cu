@@ -11,7 +11,9 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -126,7 +128,15 @@ struct pi_ffn {
     std::vector<cudaEvent_t> prof_ev;   // pairs: [2k] before, [2k+1] after launch k
     std::vector<int> prof_kind;
     size_t prof_n = 0;
-    // recorded decode step
+    // persistent decode-step kernel (batch 1)
+    bool stack_ok = false;
+    StackLayer *stack_layers = nullptr;
+    uint32_t *stack_mask = nullptr;
+    float *stack_sumsq = nullptr;
+    int stack_slots = 0, stack_slot_bytes = 0;
+    size_t stack_smem = 0;
+    int off_ring = 0, off_words = 0, off_pre = 0, off_mbar = 0, off_ua = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
+    // recorded decode step (multi-kernel path)
     cudaGraphExec_t gexec = nullptr;
     int g_B = 0;
     const float *g_x0 = nullptr;
@@ -287,6 +297,110 @@ cudaError_t enqueue_stack(const pi_ffn_t *h, const float *x0, int B, float *x_ou
 
 bool legacy_stream(cudaStream_t s) { return s == nullptr || s == cudaStreamLegacy; }
 
+// Whether the persistent decode-step kernel serves this handle at batch 1, and its
+// shared-memory layout. It is used when PI_FFN_STACK_KERNEL=1 is set in the environment.
+void plan_stack(pi_ffn_t *h)
+{
+    h->stack_ok = false;
+    const char *env = std::getenv("PI_FFN_STACK_KERNEL");
+    if (!env || env[0] != '1') return;
+    const pi_ffn_desc_t &D = h->desc;
+    const bool combo = (D.wdtype == PI_F32 && D.pdtype == PI_F32) || (D.wdtype == PI_BF16 && D.pdtype == PI_BF16) ||
+                       (D.wdtype == PI_F16 && D.pdtype == PI_F16) ||
+                       (D.wdtype == PI_INT4_G128 && (D.pdtype == PI_F16 || D.pdtype == PI_BF16));
+    if (!combo) return;
+    const int V = D.wdtype == PI_F32 ? 4 : (D.wdtype == PI_INT4_G128 ? 32 : 8);
+    const int cpt = D.wdtype == PI_INT4_G128 ? 1 : 3;
+    if (D.d % V || D.d / V > cpt * STACK_NT) return;
+    if (D.wdtype == PI_INT4_G128) {
+        if (D.d % 1024) return;                                    // scale rows must be 16-byte multiples
+        for (const pi_layer_weights_t &w : h->layers)              // and start 16-byte aligned (bulk copies)
+            if ((uintptr_t)w.s_gate % 16 || (uintptr_t)w.s_up % 16 || (uintptr_t)w.s_down % 16) return;
+    }
+    if ((long long)D.f > (long long)(STACK_MAX_CHUNK - 1) * STACK_NCHUNK) return;
+    const int P = h->nsm;
+    if ((D.f + P - 1) / P / 32 + 2 > STACK_MAX_BITWORDS) return;
+    if ((D.r + P - 1) / P > STACK_MAX_P1_ROWS) return;
+    const int rows = D.kind == PI_FFN_GATED_RELU ? 3 : 2;
+    const size_t rowb = elt_row_bytes(D.wdtype, D.d);
+    const size_t sclb = D.wdtype == PI_INT4_G128 ? (size_t)(D.d / 128) * 2 : 0;
+    const size_t slot = align_up(rows * (rowb + sclb), 128);
+    const size_t W = (size_t)(D.f + 31) / 32;
+    const size_t off_ua = 0;
+    const size_t off_hp = align_up(off_ua + (size_t)D.d * 4, 128);
+    const size_t off_scr = align_up(off_hp + (size_t)D.r * 4, 128);
+    const size_t off_words = off_scr + 8192;
+    const size_t off_pre = align_up(off_words + 4 * W, 16);
+    const size_t off_mbar = align_up(off_pre + 4 * (W + 1), 16);
+    const size_t off_ring = align_up(off_mbar + 8 * (STACK_MAX_SLOTS + 1), 128);
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    const size_t cap = (size_t)optin > 8192 ? ((size_t)optin - 6144) / 128 * 128 : 0;   // room for static arrays
+    if (off_ring + 2 * slot > cap) return;
+    const size_t ring = cap - off_ring;
+    h->stack_slots = (int)std::min((size_t)STACK_MAX_SLOTS, ring / slot);
+    h->stack_slot_bytes = (int)slot;
+    h->stack_smem = cap;
+    h->stack_ring = (int)ring;
+    h->off_ua = (int)off_ua;
+    h->off_hp = (int)off_hp;
+    h->off_scr = (int)off_scr;
+    h->off_ring = (int)off_ring;
+    h->off_words = (int)off_words;
+    h->off_pre = (int)off_pre;
+    h->off_mbar = (int)off_mbar;
+    h->stack_ok = true;
+}
+
+cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32_t *counts, int32_t *idx_out,
+                         cudaStream_t st)
+{
+    const pi_ffn_desc_t &D = h->desc;
+    StackArgs a;
+    a.layers = h->stack_layers;
+    a.L = D.n_layers;
+    a.d = D.d;
+    a.f = D.f;
+    a.r = D.r;
+    a.tau = D.tau_logit;
+    a.eps = RMS_EPS;
+    a.x0 = x0;
+    a.xa = h->xbuf[0];
+    a.xb = h->xbuf[1];
+    a.x_out = x_out;
+    a.hp = h->hp;
+    a.maskw = h->stack_mask;
+    a.part = h->part;
+    a.sumsq = h->stack_sumsq;
+    a.counts = counts;
+    a.idx_out = idx_out;
+    a.bar = reinterpret_cast<unsigned long long *>(h->tickets + 2);
+    a.status = h->status;
+    a.slots = h->stack_slots;
+    a.slot_bytes = h->stack_slot_bytes;
+    a.nblocks = (unsigned)h->nsm;
+    const long long pbytes = (D.pdtype == PI_F32 ? 4LL : 2LL) * ((long long)D.r * D.d + (long long)D.f * D.r);
+    a.pf_bytes = std::min(pbytes, 48LL << 20);
+    a.off_ua = h->off_ua;
+    a.off_hp = h->off_hp;
+    a.off_scr = h->off_scr;
+    a.off_ring = h->off_ring;
+    a.off_words = h->off_words;
+    a.off_pre = h->off_pre;
+    a.off_mbar = h->off_mbar;
+    a.ring_bytes = h->stack_ring;
+    switch (D.wdtype) {
+    case PI_F32: return launch_stack_wt<0>(D.pdtype, D.kind, a, h->nsm, h->stack_smem, st);
+    case PI_BF16: return launch_stack_wt<1>(D.pdtype, D.kind, a, h->nsm, h->stack_smem, st);
+    case PI_F16: return launch_stack_wt<2>(D.pdtype, D.kind, a, h->nsm, h->stack_smem, st);
+    case PI_INT4_G128: return launch_stack_wt<3>(D.pdtype, D.kind, a, h->nsm, h->stack_smem, st);
+    }
+    return cudaErrorNotSupported;
+}
+
 }  // namespace
 
 extern "C" {
@@ -347,6 +461,9 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
         (size_t)D.f * 4,                               // idx_ws
         4,                                             // count_ws
         (size_t)D.n_layers * 4,                        // counts_ws
+        (size_t)D.n_layers * sizeof(StackLayer),       // stack_layers
+        (size_t)D.n_layers * ((D.f + 31) / 32) * 4,    // stack_mask
+        (size_t)(D.d + STACK_SLICE - 1) / STACK_SLICE * 4,  // stack_sumsq
     };
     const int nbuf = sizeof(sizes) / sizeof(sizes[0]);
     size_t off[16], total = 0;
@@ -377,6 +494,24 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
     h->idx_ws = (int32_t *)(base + off[10]);
     h->count_ws = (int32_t *)(base + off[11]);
     h->counts_ws = (int32_t *)(base + off[12]);
+    h->stack_layers = (StackLayer *)(base + off[13]);
+    h->stack_mask = (uint32_t *)(base + off[14]);
+    h->stack_sumsq = (float *)(base + off[15]);
+    {
+        std::vector<StackLayer> sl(D.n_layers);
+        for (int l = 0; l < D.n_layers; ++l) {
+            const pi_layer_weights_t &w = h->layers[l];
+            sl[l] = StackLayer{w.w_gate, w.w_up, w.w_down_t, w.s_gate, w.s_up, w.s_down, w.b_gate, w.p1_t, w.p2_t,
+                               w.b_pred};
+        }
+        if ((s = cuda_status(cudaMemcpy(h->stack_layers, sl.data(), sl.size() * sizeof(StackLayer),
+                                        cudaMemcpyHostToDevice))) != PI_OK) {
+            cudaFree(h->ws);
+            delete h;
+            return s;
+        }
+    }
+    plan_stack(h);
     *out = h;
     return PI_OK;
 }
@@ -428,6 +563,15 @@ pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_ou
     if ((s = check_opt(counts, (size_t)D.n_layers * 4, 4, h->dev))) return s;
     if ((s = check_opt(idx_out, (size_t)D.n_layers * D.f * 4, 4, h->dev))) return s;
     cudaStream_t st = (cudaStream_t)stream;
+
+    if (B == 1 && h->stack_ok) {
+        ProfScope p(h, st, PI_K_STACK);
+        cudaError_t e = launch_stack(h, x0, x_out, counts, idx_out, st);
+        if (e == cudaSuccess) return PI_OK;
+        cudaGetLastError();
+        if (e != cudaErrorNotSupported && e != cudaErrorCooperativeLaunchTooLarge) return cuda_status(e);
+        h->stack_ok = false;   // not launchable here: use the multi-kernel path from now on
+    }
 
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (!legacy_stream(st) && cudaStreamIsCapturing(st, &cs) != cudaSuccess) return cuda_status(cudaGetLastError());
@@ -506,6 +650,8 @@ pi_status_t pi_get_status(pi_ffn_t *h)
     uint32_t v = 0;
     if (cudaMemcpy(&v, h->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_status(cudaGetLastError());
     if (v && cudaMemset(h->status, 0, 4) != cudaSuccess) return cuda_status(cudaGetLastError());
+    // a grid barrier that gave up leaves its arrival count behind: start the next step clean
+    if (v == PI_ERR_TIMEOUT && cudaMemset(h->tickets + 2, 0, 8) != cudaSuccess) return cuda_status(cudaGetLastError());
     return (pi_status_t)v;
 }
 

@@ -1,0 +1,160 @@
+// pi_async.cuh -- bulk asynchronous copies, mbarriers, L2 prefetch and a bounded grid barrier (sm_103a).
+//
+// Every wait here is bounded by the global nanosecond timer: on expiry the
+// caller gets `false`, records PI_ERR_TIMEOUT in the status word and leaves.
+#pragma once
+
+#include "pi_common.cuh"
+
+namespace pi {
+
+constexpr unsigned long long WAIT_LIMIT_NS = 200ull * 1000 * 1000;   // 200 ms
+
+__device__ __forceinline__ unsigned long long globaltimer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// ---------------------------------------------------------------- mbarrier -------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_inval(uint64_t *bar)
+{
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Make initialised barriers visible to the async proxy (bulk copies complete on them).
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order this thread's generic-proxy shared-memory accesses (and, after a CTA barrier,
+// those of the threads it synchronised with) before its later async-proxy ones.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of the barrier to complete; false after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    return true;
+}
+
+// ---------------------------------------------------------------- bulk copies ----------------
+
+// global -> shared, `bytes` (multiple of 16, both addresses 16-byte aligned); completion
+// is signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Bring `bytes` (multiple of 16, 16-byte aligned) of global memory into L2 without waiting.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2_range(const void *src, size_t bytes)
+{
+    const char *p = (const char *)src;
+    bytes &= ~(size_t)15;
+    while (bytes > 0) {
+        const uint32_t n = bytes > (64u << 10) ? (64u << 10) : (uint32_t)bytes;
+        prefetch_l2(p, n);
+        p += n;
+        bytes -= n;
+    }
+}
+
+// ---------------------------------------------------------------- grid barrier ---------------
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_add_u64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Monotonic grid barrier: every arrival adds 1 to a 64-bit counter (no reply awaited),
+// and the k-th barrier of a launch completes when the counter reaches base + k * nblocks.
+// A launch that passes all its barriers leaves the counter at a multiple of
+// (barriers per launch * nblocks), which is how the next launch finds its base.
+__device__ __forceinline__ unsigned long long barrier_base(const unsigned long long *cnt, unsigned long long per_launch)
+{
+    const unsigned long long c = ld_acquire_u64(cnt);
+    return c - c % per_launch;
+}
+
+// Returns false in every thread of a CTA that gave up waiting (after recording PI_ERR_TIMEOUT).
+__device__ __forceinline__ bool grid_sync_to(unsigned long long *cnt, unsigned long long target, uint32_t *status,
+                                             int *s_flag)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        __threadfence();
+        red_release_add_u64(cnt, 1ull);
+        if ((long long)(ld_acquire_u64(cnt) - target) < 0) {
+            const unsigned long long t0 = globaltimer_ns();
+            while ((long long)(ld_acquire_u64(cnt) - target) < 0) {
+                if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                    set_status(status, ST_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+        *s_flag = ok;
+    }
+    __syncthreads();
+    return *s_flag != 0;
+}
+
+}  // namespace pi

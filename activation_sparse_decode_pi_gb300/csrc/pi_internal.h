@@ -18,6 +18,50 @@ constexpr int DOWN_GROUP_MIN = 16;    // smallest group of active neurons per fp
 constexpr int MAX_GROUPS = 256;       // at most this many partials per layer (group size grows with the count)
 constexpr size_t SMEM_VEC_CAP = 96 * 1024;  // shared memory for one staged batch tile of input vectors
 
+// Persistent decode-step kernel (batch 1): one CTA of STACK_NT threads per SM.
+constexpr int STACK_NT = 512;
+constexpr int STACK_NCHUNK = 152;         // fixed partition of a layer's active list into fp32 partials
+constexpr int STACK_SLICE = 32;           // output columns per reduction slice
+constexpr int STACK_MAX_CHUNK = 512;      // neurons one chunk may hold (f <= 511 * STACK_NCHUNK)
+constexpr int STACK_MAX_BITWORDS = 24;    // mask words one CTA's logit rows may touch
+constexpr int STACK_MAX_SLOTS = 16;       // shared-memory ring slots (one neuron's rows each)
+constexpr int STACK_MAX_P1_ROWS = 8;      // predictor hidden units one CTA owns (r <= 8 * SMs)
+
+struct StackLayer {
+    const void *wg, *wu, *wd;     // [f x d] gate (W1), up (NULL if non-gated), W_down transposed
+    const void *sg, *su, *sd;     // int4 scales or NULL
+    const float *bg;              // gate bias or NULL
+    const void *p1, *p2;          // predictor [r x d], [f x r]
+    const float *bp;              // predictor bias or NULL
+};
+
+struct StackArgs {
+    const StackLayer *layers;     // device array [L]
+    int L, d, f, r;
+    float tau, eps;
+    const float *x0;
+    float *xa, *xb, *x_out;       // ping-pong layer outputs, final output
+    float *hp;                    // [r]
+    uint32_t *maskw;              // [L x ceil(f/32)], zeroed by the kernel
+    float *part;                  // [STACK_NCHUNK x d]
+    float *sumsq;                 // [ceil(d/STACK_SLICE)]
+    int32_t *counts, *idx_out;    // optional outputs
+    unsigned long long *bar;      // monotonic grid-barrier counter (zeroed at create and after a timeout)
+    uint32_t *status;
+    int slots, slot_bytes;
+    unsigned nblocks;             // CTAs expected at every grid barrier
+    long long pf_bytes;           // next-layer predictor bytes to prefetch into L2
+    int off_ua, off_hp, off_scr, off_words, off_pre, off_mbar, off_ring;   // dynamic shared-memory layout
+    int ring_bytes;               // ring region: next layer's P2 slice, then the row slots
+};
+
+template <int WT>
+cudaError_t launch_stack_wt(int pdt, int kind, const StackArgs &a, int grid, size_t smem, cudaStream_t s);
+extern template cudaError_t launch_stack_wt<0>(int, int, const StackArgs &, int, size_t, cudaStream_t);
+extern template cudaError_t launch_stack_wt<1>(int, int, const StackArgs &, int, size_t, cudaStream_t);
+extern template cudaError_t launch_stack_wt<2>(int, int, const StackArgs &, int, size_t, cudaStream_t);
+extern template cudaError_t launch_stack_wt<3>(int, int, const StackArgs &, int, size_t, cudaStream_t);
+
 struct Launch {
     dim3 grid, block;     // grid.x == 0: persistent grid, one wave of resident CTAs over nsm SMs
     size_t smem;

@@ -140,8 +140,13 @@ pi_status_t pi_sparse_ffn(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
  * x0: [B x d] fp32 device; x_out: [B x d] fp32 device, out (= x_L).
  * counts: [n_layers] int32 device out (active count per layer), or NULL.
  * idx_out: [n_layers x f] int32 device out (layer l's ascending active list in row l), or NULL.
- * No host synchronisation inside. Outside stream capture the step is recorded once
- * into a CUDA graph per (B, pointer set) and replayed.
+ * No host synchronisation inside. Outside stream capture the multi-kernel step is
+ * recorded once into a CUDA graph per (B, pointer set) and replayed. With
+ * PI_FFN_STACK_KERNEL=1 in the environment at pi_ffn_create, B = 1 steps (element-type
+ * pairs f32/f32, bf16/bf16, f16/f16, int4/f16, int4/bf16, when the shapes fit its
+ * shared-memory plan) instead run as ONE persistent cooperative kernel, one CTA per SM,
+ * whose layers are separated by bounded grid barriers; a barrier that gives up records
+ * PI_ERR_TIMEOUT.
  */
 pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_out,
                             int32_t *counts, int32_t *idx_out, void *stream);
@@ -178,7 +183,8 @@ typedef enum {
     PI_K_FFN_H = 3,        /* gate/up gather-GEMV */
     PI_K_FFN_DOWN = 4,     /* row-sparse W_down axpy into fp32 partials */
     PI_K_REDUCE = 5,       /* deterministic reduction (+ residual, next RMS scale) */
-    PI_K_COUNT = 6
+    PI_K_STACK = 6,        /* persistent decode step, all layers in one kernel (batch 1) */
+    PI_K_COUNT = 7
 } pi_kernel_kind_t;
 
 pi_status_t pi_profile_begin(pi_ffn_t *h);
@@ -210,6 +216,16 @@ pi_status_t pi_profile_end(pi_ffn_t *h, float *ms, int32_t *launches, int32_t n_
 pi_status_t pi_sparse_ffn_noalloc(const pi_ffn_desc_t *desc, const pi_layer_weights_t *layer,
                                   const float *u, int32_t B, const int32_t *idx, const int32_t *count,
                                   float *y, int32_t *status, void *stream);
+
+/*
+ * Failure-detection self-test of the bounded grid barrier used by pi_decode_stack.
+ * work: 4 zeroed uint32 words of device memory, 8-byte aligned: [0..1] barrier counter, [2] number of
+ * CTAs that passed the barrier, [3] status out. A cooperative grid of 2 CTAs meets at
+ * the barrier expecting 2 + extra CTAs. extra = 0: both pass, work[2] = 2, work[3] = 0.
+ * extra > 0: no CTA can pass; each gives up after the barrier's limit (200 ms),
+ * work[3] = PI_ERR_TIMEOUT, and the kernel returns (no trap, the context stays usable).
+ */
+pi_status_t pi_selftest_grid_barrier(uint32_t *work, int32_t extra, void *stream);
 
 /* Wait for all work on the device, return the first kernel-recorded error and clear it. */
 pi_status_t pi_get_status(pi_ffn_t *h);

@@ -253,3 +253,83 @@ def test_decode_stack_under_user_capture(P):
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
     ffn.close()
+
+
+# ------------------------------------------------------------------ persistent decode-step kernel
+
+STACK_SHAPE = dict(d=2048, f=3001, r=136)   # int4 rows need d % 1024 == 0 on this path
+
+
+def _handle(P, w, layers, stack_kernel: bool):
+    import os
+
+    old = os.environ.get("PI_FFN_STACK_KERNEL")
+    os.environ["PI_FFN_STACK_KERNEL"] = "1" if stack_kernel else "0"
+    try:
+        return P.SparseFFN.from_workload(w, layers, max_batch=1)
+    finally:
+        if old is None:
+            del os.environ["PI_FFN_STACK_KERNEL"]
+        else:
+            os.environ["PI_FFN_STACK_KERNEL"] = old
+
+
+@pytest.mark.parametrize("wi", range(5))
+def test_decode_stack_both_paths_batch1(P, wi):
+    """Batch 1: the single persistent kernel and the multi-kernel step both match the oracle."""
+    w = _wl(wi, STACK_SHAPE, n_layers=3)
+    layers = build_layers(w, range(w.n_layers))
+    X = make_inputs(w, 2, 1, seed=5, device="cpu").numpy()
+    for stack_kernel in (True, False):
+        ffn = _handle(P, w, [g for g, _ in layers], stack_kernel)
+        for t in range(X.shape[0]):
+            counts = torch.zeros(w.n_layers, dtype=torch.int32, device="cuda")
+            idx_out = torch.zeros((w.n_layers, w.f), dtype=torch.int32, device="cuda")
+            P.pi_profile_begin(ffn.h)
+            xo = ffn.decode_stack(to_dev(X[t]), counts=counts, idx_out=idx_out)
+            prof = P.pi_profile_end(ffn.h)
+            if stack_kernel:
+                assert prof["decode_stack"][1] == 1 and prof["ffn_h"][1] == 0, prof
+            else:
+                assert prof["decode_stack"][1] == 0 and prof["ffn_h"][1] == w.n_layers, prof
+            xo2 = ffn.decode_stack(to_dev(X[t]), counts=counts, idx_out=idx_out).clone()
+            torch.cuda.synchronize()
+            assert torch.equal(xo, xo2), "decode step is not deterministic"
+            st = oracle.stack(X[t].astype(np.float64), [o for _, o in layers], w.kind, w.wdtype, w.pdtype)
+            cg, ig = counts.cpu().numpy(), idx_out.cpu().numpy()
+            same = True
+            for l in range(w.n_layers):
+                gi = ig[l, : cg[l]]
+                assert np.all(np.diff(gi) > 0)
+                diff = np.setxor1d(gi, st["idx"][l])
+                if diff.size:
+                    assert np.all(st["zmin"][l][diff] < oracle.BAND), (stack_kernel, l, diff)
+                    same = False
+                    break
+            if same:
+                err = rel_l2(xo.cpu().numpy() - X[t], st["x_out"] - X[t])
+                assert err <= TOL[w.wdtype], (stack_kernel, err)
+        assert ffn.status() == 0
+        ffn.close()
+
+
+def test_grid_barrier_gives_up_cleanly(P):
+    """A barrier that can never complete times out, reports PI_ERR_TIMEOUT, and the GPU stays usable."""
+    work = torch.zeros(4, dtype=torch.int32, device="cuda")
+    P.pi_selftest_grid_barrier(work, 0)
+    torch.cuda.synchronize()
+    assert work.cpu().tolist()[2:] == [2, 0]
+    work.zero_()
+    P.pi_selftest_grid_barrier(work, 1)
+    torch.cuda.synchronize()
+    assert work.cpu().tolist()[2:] == [0, P.PI_ERR_TIMEOUT]
+    # the context still runs a decode step afterwards
+    w = _wl(1, SMALL, n_layers=1)
+    (Lg, Lo), = build_layers(w, [0])
+    ffn = P.SparseFFN.from_workload(w, [Lg], max_batch=1)
+    x0 = to_dev(make_inputs(w, 1, 1).numpy()[0])
+    xo = ffn.decode_stack(x0)
+    torch.cuda.synchronize()
+    assert torch.isfinite(xo).all()
+    assert ffn.status() == 0
+    ffn.close()
