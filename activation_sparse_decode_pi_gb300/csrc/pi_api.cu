@@ -135,7 +135,7 @@ struct pi_ffn {
     float *stack_sumsq = nullptr;
     int stack_slots = 0, stack_slot_bytes = 0;
     size_t stack_smem = 0;
-    int off_ring = 0, off_words = 0, off_pre = 0, off_mbar = 0, off_ua = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
+    int off_ring = 0, off_flags = 0, off_mbar = 0, off_ua = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
     // recorded decode step (multi-kernel path)
     cudaGraphExec_t gexec = nullptr;
     int g_B = 0;
@@ -298,12 +298,12 @@ cudaError_t enqueue_stack(const pi_ffn_t *h, const float *x0, int B, float *x_ou
 bool legacy_stream(cudaStream_t s) { return s == nullptr || s == cudaStreamLegacy; }
 
 // Whether the persistent decode-step kernel serves this handle at batch 1, and its
-// shared-memory layout. It is used when PI_FFN_STACK_KERNEL=1 is set in the environment.
+// shared-memory layout. PI_FFN_STACK_KERNEL=0 in the environment turns it off.
 void plan_stack(pi_ffn_t *h)
 {
     h->stack_ok = false;
     const char *env = std::getenv("PI_FFN_STACK_KERNEL");
-    if (!env || env[0] != '1') return;
+    if (env && env[0] == '0') return;
     const pi_ffn_desc_t &D = h->desc;
     const bool combo = (D.wdtype == PI_F32 && D.pdtype == PI_F32) || (D.wdtype == PI_BF16 && D.pdtype == PI_BF16) ||
                        (D.wdtype == PI_F16 && D.pdtype == PI_F16) ||
@@ -317,40 +317,40 @@ void plan_stack(pi_ffn_t *h)
         for (const pi_layer_weights_t &w : h->layers)              // and start 16-byte aligned (bulk copies)
             if ((uintptr_t)w.s_gate % 16 || (uintptr_t)w.s_up % 16 || (uintptr_t)w.s_down % 16) return;
     }
-    if ((long long)D.f > (long long)(STACK_MAX_CHUNK - 1) * STACK_NCHUNK) return;
     const int P = h->nsm;
-    if ((D.f + P - 1) / P / 32 + 2 > STACK_MAX_BITWORDS) return;
+    if (P > MAX_GROUPS) return;                                   // one fp32 partial per CTA
+    if ((D.f + P - 1) / P > STACK_MAX_CHUNK) return;
     if ((D.r + P - 1) / P > STACK_MAX_P1_ROWS) return;
+    for (const pi_layer_weights_t &w : h->layers)                  // gate bias may travel as a 16-byte chunk
+        if ((uintptr_t)w.b_gate % 16) return;
     const int rows = D.kind == PI_FFN_GATED_RELU ? 3 : 2;
     const size_t rowb = elt_row_bytes(D.wdtype, D.d);
     const size_t sclb = D.wdtype == PI_INT4_G128 ? (size_t)(D.d / 128) * 2 : 0;
-    const size_t slot = align_up(rows * (rowb + sclb), 128);
-    const size_t W = (size_t)(D.f + 31) / 32;
+    const size_t slot = align_up(rows * (rowb + sclb) + 16, 128);
+    const size_t own = (size_t)(D.f + P - 1) / P;
     const size_t off_ua = 0;
     const size_t off_hp = align_up(off_ua + (size_t)D.d * 4, 128);
     const size_t off_scr = align_up(off_hp + (size_t)D.r * 4, 128);
-    const size_t off_words = off_scr + 8192;
-    const size_t off_pre = align_up(off_words + 4 * W, 16);
-    const size_t off_mbar = align_up(off_pre + 4 * (W + 1), 16);
-    const size_t off_ring = align_up(off_mbar + 8 * (STACK_MAX_SLOTS + 1), 128);
+    const size_t off_flags = off_scr + 8192;
+    const size_t off_mbar = align_up(off_flags + own, 16);
+    const size_t off_ring = align_up(off_mbar + 8 * STACK_MAX_SLOTS, 128);
     int optin = 0;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev) != cudaSuccess) {
         cudaGetLastError();
         return;
     }
-    const size_t cap = (size_t)optin > 8192 ? ((size_t)optin - 6144) / 128 * 128 : 0;   // room for static arrays
+    const size_t cap = (size_t)optin > 8192 ? ((size_t)optin - 8192) / 128 * 128 : 0;   // room for static arrays
     if (off_ring + 2 * slot > cap) return;
     const size_t ring = cap - off_ring;
     h->stack_slots = (int)std::min((size_t)STACK_MAX_SLOTS, ring / slot);
     h->stack_slot_bytes = (int)slot;
-    h->stack_smem = cap;
-    h->stack_ring = (int)ring;
+    h->stack_smem = off_ring + (size_t)h->stack_slots * slot;
+    h->stack_ring = (int)((size_t)h->stack_slots * slot);
     h->off_ua = (int)off_ua;
     h->off_hp = (int)off_hp;
     h->off_scr = (int)off_scr;
     h->off_ring = (int)off_ring;
-    h->off_words = (int)off_words;
-    h->off_pre = (int)off_pre;
+    h->off_flags = (int)off_flags;
     h->off_mbar = (int)off_mbar;
     h->stack_ok = true;
 }
@@ -388,10 +388,12 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.off_hp = h->off_hp;
     a.off_scr = h->off_scr;
     a.off_ring = h->off_ring;
-    a.off_words = h->off_words;
-    a.off_pre = h->off_pre;
+    a.off_flags = h->off_flags;
     a.off_mbar = h->off_mbar;
     a.ring_bytes = h->stack_ring;
+    a.bias_bulk = D.f % 4 == 0 ? 1 : 0;
+    for (const pi_layer_weights_t &w : h->layers)
+        if (!w.b_gate) a.bias_bulk = 0;
     switch (D.wdtype) {
     case PI_F32: return launch_stack_wt<0>(D.pdtype, D.kind, a, h->nsm, h->stack_smem, st);
     case PI_BF16: return launch_stack_wt<1>(D.pdtype, D.kind, a, h->nsm, h->stack_smem, st);

@@ -138,8 +138,7 @@ __device__ __forceinline__ bool grid_sync_to(unsigned long long *cnt, unsigned l
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
-        __threadfence();
-        red_release_add_u64(cnt, 1ull);
+        red_release_add_u64(cnt, 1ull);   // release: the CTA's writes before the CTA barrier
         if ((long long)(ld_acquire_u64(cnt) - target) < 0) {
             const unsigned long long t0 = globaltimer_ns();
             while ((long long)(ld_acquire_u64(cnt) - target) < 0) {
@@ -148,10 +147,10 @@ __device__ __forceinline__ bool grid_sync_to(unsigned long long *cnt, unsigned l
                     ok = 0;
                     break;
                 }
+                __nanosleep(64);   // fewer polls on the counter's line while the arrivals land
             }
         }
-        __threadfence();
-        *s_flag = ok;
+        *s_flag = ok;                      // the acquiring load above orders what follows
     }
     __syncthreads();
     return *s_flag != 0;

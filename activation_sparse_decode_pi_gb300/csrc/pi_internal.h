@@ -20,10 +20,8 @@ constexpr size_t SMEM_VEC_CAP = 96 * 1024;  // shared memory for one staged batc
 
 // Persistent decode-step kernel (batch 1): one CTA of STACK_NT threads per SM.
 constexpr int STACK_NT = 512;
-constexpr int STACK_NCHUNK = 152;         // fixed partition of a layer's active list into fp32 partials
 constexpr int STACK_SLICE = 32;           // output columns per reduction slice
-constexpr int STACK_MAX_CHUNK = 512;      // neurons one chunk may hold (f <= 511 * STACK_NCHUNK)
-constexpr int STACK_MAX_BITWORDS = 24;    // mask words one CTA's logit rows may touch
+constexpr int STACK_MAX_CHUNK = 512;      // neurons one CTA may own (f <= 512 * grid)
 constexpr int STACK_MAX_SLOTS = 16;       // shared-memory ring slots (one neuron's rows each)
 constexpr int STACK_MAX_P1_ROWS = 8;      // predictor hidden units one CTA owns (r <= 8 * SMs)
 
@@ -43,7 +41,7 @@ struct StackArgs {
     float *xa, *xb, *x_out;       // ping-pong layer outputs, final output
     float *hp;                    // [r]
     uint32_t *maskw;              // [L x ceil(f/32)], zeroed by the kernel
-    float *part;                  // [STACK_NCHUNK x d]
+    float *part;                  // [grid x d] one fp32 partial per CTA
     float *sumsq;                 // [ceil(d/STACK_SLICE)]
     int32_t *counts, *idx_out;    // optional outputs
     unsigned long long *bar;      // monotonic grid-barrier counter (zeroed at create and after a timeout)
@@ -51,8 +49,9 @@ struct StackArgs {
     int slots, slot_bytes;
     unsigned nblocks;             // CTAs expected at every grid barrier
     long long pf_bytes;           // next-layer predictor bytes to prefetch into L2
-    int off_ua, off_hp, off_scr, off_words, off_pre, off_mbar, off_ring;   // dynamic shared-memory layout
-    int ring_bytes;               // ring region: next layer's P2 slice, then the row slots
+    int off_ua, off_hp, off_scr, off_flags, off_mbar, off_ring;   // dynamic shared-memory layout
+    int ring_bytes;               // ring region: the neuron slots
+    int bias_bulk;                // gate biases ride in the row copies (every layer has one and f % 4 == 0)
 };
 
 template <int WT>

@@ -75,6 +75,31 @@ __device__ __forceinline__ void rows_consume(const RowChunks<DT, RW, U> &rc, int
             for (int k = 0; k < RW; ++k)
 #pragma unroll
                 for (int b = 0; b < BT; ++b) acc[k][b] = fmaf(rc.s[k][i], part[k][b], acc[k][b]);
+        } else if constexpr (RW > BT) {
+            // more rows than batch rows: hold the chunk of u, stream the rows through one at a time
+            float uv[BT][V];
+#pragma unroll
+            for (int b = 0; b < BT; ++b)
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    const float4 u = su4[b * (K / 4) + q * nch + ci];
+                    uv[b][4 * q + 0] = u.x;
+                    uv[b][4 * q + 1] = u.y;
+                    uv[b][4 * q + 2] = u.z;
+                    uv[b][4 * q + 3] = u.w;
+                }
+#pragma unroll
+            for (int k = 0; k < RW; ++k) {
+                float wf[V];
+                unpack<DT>(rc.w[k][i], wf);
+#pragma unroll
+                for (int b = 0; b < BT; ++b) {
+                    float a = acc[k][b];
+#pragma unroll
+                    for (int e = 0; e < V; ++e) a = fmaf(wf[e], uv[b][e], a);
+                    acc[k][b] = a;
+                }
+            }
         } else {
             float wf[RW][V];
 #pragma unroll

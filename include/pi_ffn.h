@@ -140,13 +140,14 @@ pi_status_t pi_sparse_ffn(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
  * x0: [B x d] fp32 device; x_out: [B x d] fp32 device, out (= x_L).
  * counts: [n_layers] int32 device out (active count per layer), or NULL.
  * idx_out: [n_layers x f] int32 device out (layer l's ascending active list in row l), or NULL.
- * No host synchronisation inside. Outside stream capture the multi-kernel step is
- * recorded once into a CUDA graph per (B, pointer set) and replayed. With
- * PI_FFN_STACK_KERNEL=1 in the environment at pi_ffn_create, B = 1 steps (element-type
- * pairs f32/f32, bf16/bf16, f16/f16, int4/f16, int4/bf16, when the shapes fit its
- * shared-memory plan) instead run as ONE persistent cooperative kernel, one CTA per SM,
- * whose layers are separated by bounded grid barriers; a barrier that gives up records
- * PI_ERR_TIMEOUT.
+ * No host synchronisation inside. B = 1 steps (element-type pairs f32/f32, bf16/bf16,
+ * f16/f16, int4/f16, int4/bf16, when the shapes fit its shared-memory plan) run as ONE
+ * persistent cooperative kernel, one CTA per SM, whose layers are separated by bounded
+ * grid barriers; a barrier that gives up records PI_ERR_TIMEOUT. Its partial sums are
+ * one per CTA, so the output bits depend on the SM count (and nothing else).
+ * PI_FFN_STACK_KERNEL=0 in the environment at pi_ffn_create turns it off. Other steps
+ * run as a chain of kernels, recorded once outside stream capture into a CUDA graph
+ * per (B, pointer set) and replayed.
  */
 pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_out,
                             int32_t *counts, int32_t *idx_out, void *stream);
