@@ -36,6 +36,35 @@ sys.path.insert(0, ROOT)
 from workload import WORKLOADS, make_inputs, make_layer  # noqa: E402
 
 DEFAULT_WORKLOAD = "relullama7b_d4096_f11008_bf16_L32"
+CSRC = os.path.join(ROOT, "activation_sparse_decode_pi_gb300", "csrc")
+
+# DRAM traffic of the dominant kernel per launch, from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), with a hash of the kernel sources it was taken on. The capture ran a
+# 4-layer slice of the workload; traffic grows in proportion to layers, so it is kept per layer.
+# A source change makes the recorded figure stale and the bench then reports null.
+NCU_TRAFFIC = {
+    ("relullama7b_d4096_f11008_bf16_L32", "decode_stack"): {"bytes_per_layer": 238313216 / 4,
+                                                            "csrc": "04668426e57d3363"},
+}
+
+
+def csrc_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(CSRC, name), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(w, kernel: str):
+    rec = NCU_TRAFFIC.get((w.name, kernel))
+    if not rec or rec["csrc"] != csrc_hash():
+        return None
+    return rec["bytes_per_layer"] * w.n_layers
 METRIC = "sparse-FFN decode tokens/s (batch 1) and achieved HBM GB/s vs peak on GB300"
 POOL_TOKENS = 256
 WB = {"f32": 4.0, "bf16": 2.0, "f16": 2.0, "int4g128": 0.5}
@@ -366,7 +395,7 @@ def run_ours(args):
         "bytes_per_step": bytes_per_step,
         "mean_active_per_layer": mean_count,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": ncu_traffic(w, dom), "algorithmic_bytes": dom_bytes,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s"},
         "kernels": kernel_table,
