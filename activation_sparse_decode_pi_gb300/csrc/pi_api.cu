@@ -136,6 +136,16 @@ struct pi_ffn {
     int stack_slots = 0, stack_slot_bytes = 0;
     size_t stack_smem = 0;
     int off_ring = 0, off_flags = 0, off_mbar = 0, off_ua = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
+    // tensor-core path (batch >= tc_min_b)
+    bool tc_ok = false;
+    int tc_min_b = 16, tc_nbmax = 0, tc_rpad = 0, tc_fpad = 0;
+    int tc_stages[5][4] = {};          // [mode][log2(NB / 16)]
+    size_t tc_smem[5][4] = {};
+    uint16_t *tc_uhi = nullptr, *tc_ulo = nullptr, *tc_hphi = nullptr, *tc_hplo = nullptr, *tc_hhi = nullptr,
+             *tc_hlo = nullptr;
+    float *tc_part = nullptr;
+    uint32_t *tc_cnt = nullptr;        // [tc_ntiles] tile tickets, then one done counter
+    int tc_ntiles = 0;
     // recorded decode step (multi-kernel path)
     cudaGraphExec_t gexec = nullptr;
     int g_B = 0;
@@ -274,10 +284,195 @@ cudaError_t enqueue_ffn(const pi_ffn_t *h, int layer, const float *x, const floa
                          h->inv_rms, RMS_EPS);
 }
 
+// ---------------------------------------------------------------- tensor-core path ----------
+
+int tc_nb(int B) { return B <= 16 ? 16 : B <= 32 ? 32 : B <= 64 ? 64 : 128; }
+int tc_nbi(int nb) { return nb == 16 ? 0 : nb == 32 ? 1 : nb == 64 ? 2 : 3; }
+
+bool tc_use(const pi_ffn_t *h, int B) { return h->tc_ok && B >= h->tc_min_b && B <= h->tc_nbmax; }
+
+// Whether the tensor-core kernels serve batches >= tc_min_b on this handle (16-bit weights
+// and predictor of one type, d % 128 == 0, r % 64 == 0), and their shared-memory rings.
+// PI_FFN_TC=0 turns the path off; PI_FFN_TC_MIN_BATCH moves its lower batch bound.
+void plan_tc(pi_ffn_t *h)
+{
+    h->tc_ok = false;
+    const pi_ffn_desc_t &D = h->desc;
+    const char *env = std::getenv("PI_FFN_TC");
+    if (env && env[0] == '0') return;
+    if (const char *mb = std::getenv("PI_FFN_TC_MIN_BATCH")) {
+        const int v = std::atoi(mb);
+        if (v >= 1) h->tc_min_b = v;
+    }
+    if (!((D.wdtype == PI_BF16 && D.pdtype == PI_BF16) || (D.wdtype == PI_F16 && D.pdtype == PI_F16))) return;
+    if (D.d % 128 || D.r % 64 || D.max_batch < h->tc_min_b) return;
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    const size_t avail = (size_t)optin > 2048 ? (size_t)optin - 2048 : 0;   // alignment slack + static barriers
+    for (int mode = 0; mode < 5; ++mode)
+        for (int i = 0; i < 4; ++i) {
+            const int nb = 16 << i;
+            const size_t stage = (mode == TC_GATED ? 2 : 1) * 16384 + 2 * (size_t)nb * 128;
+            const int st = (int)std::min<size_t>(TC_MAX_STAGES, avail / stage);
+            if (st < 2) return;
+            h->tc_stages[mode][i] = st;
+            h->tc_smem[mode][i] = 1024 + (size_t)st * stage;
+        }
+    h->tc_nbmax = tc_nb(std::min(D.max_batch, 128));
+    h->tc_rpad = (D.r + 127) / 128 * 128;
+    h->tc_fpad = (D.f + 127) / 128 * 128;
+    h->tc_ntiles = std::max(h->tc_fpad / 128, std::max(h->tc_rpad / 128, D.d / 128));
+    h->tc_ok = true;
+}
+
+cudaError_t tc_launch(const pi_ffn_t *h, int mode, int nb, const TcArgs &a0, cudaStream_t s, bool pdl)
+{
+    TcArgs a = a0;
+    const int i = tc_nbi(nb);
+    a.stages = h->tc_stages[mode][i];
+    a.part = h->tc_part;
+    a.tile_cnt = h->tc_cnt;
+    a.done_cnt = h->tc_cnt + h->tc_ntiles;
+    a.status = h->status;
+    return h->desc.wdtype == PI_BF16 ? launch_tc_wt<1>(mode, nb, a, h->nsm, h->tc_smem[mode][i], s, pdl)
+                                     : launch_tc_wt<2>(mode, nb, a, h->nsm, h->tc_smem[mode][i], s, pdl);
+}
+
+// u (or x_l with rms) -> uhi, ulo [NB x d]
+cudaError_t tc_split(const pi_ffn_t *h, const float *x, int B, int rms, cudaStream_t s, bool pdl)
+{
+    const pi_ffn_desc_t &D = h->desc;
+    const int nb = tc_nb(B);
+    ProfScope p(h, s, PI_K_RMS);
+    return D.wdtype == PI_BF16
+               ? launch_tc_split_wt<1>(x, D.d, B, nb, D.d, rms, RMS_EPS, h->tc_uhi, h->tc_ulo, s, pdl && !h->prof)
+               : launch_tc_split_wt<2>(x, D.d, B, nb, D.d, rms, RMS_EPS, h->tc_uhi, h->tc_ulo, s, pdl && !h->prof);
+}
+
+TcArgs tc_args()
+{
+    TcArgs a;
+    std::memset(&a, 0, sizeof(a));
+    return a;
+}
+
+// predictor on the tensor cores: hidden (P1T rows, K = d) then logits + mask + compaction (P2T rows, K = r)
+cudaError_t tc_predict(const pi_ffn_t *h, int layer, int B, int32_t *idx, int32_t *count, cudaStream_t s)
+{
+    const pi_ffn_desc_t &D = h->desc;
+    const pi_layer_weights_t &w = h->layers[layer];
+    const int nb = tc_nb(B);
+    const bool pdl = !h->prof;
+    cudaError_t e;
+    {
+        TcArgs a = tc_args();
+        a.w0 = (const uint16_t *)w.p1_t;
+        a.n_static = D.r;
+        a.f = D.r;
+        a.K = D.d;
+        a.d = D.d;
+        a.xhi = h->tc_uhi;
+        a.xlo = h->tc_ulo;
+        a.ldx = D.d;
+        a.B = B;
+        a.ohi = h->tc_hphi;
+        a.olo = h->tc_hplo;
+        a.ldo = h->tc_rpad;
+        ProfScope p(h, s, PI_K_PRED_HIDDEN);
+        e = tc_launch(h, TC_PRED_HIDDEN, nb, a, s, pdl);
+    }
+    if (e != cudaSuccess) return e;
+    TcArgs a = tc_args();
+    a.w0 = (const uint16_t *)w.p2_t;
+    a.n_static = D.f;
+    a.f = D.f;
+    a.K = D.r;
+    a.d = D.d;
+    a.xhi = h->tc_hphi;
+    a.xlo = h->tc_hplo;
+    a.ldx = h->tc_rpad;
+    a.B = B;
+    a.bias = w.b_pred;
+    a.tau = D.tau_logit;
+    a.maskw = h->maskw;
+    a.idx_out = idx;
+    a.count_out = count;
+    ProfScope p(h, s, PI_K_PRED_LOGITS);
+    return tc_launch(h, TC_LOGITS, nb, a, s, pdl);
+}
+
+// FFN on the tensor cores: h for the listed neurons (gate/up or fc1 rows, K = d), then
+// out = xin + h . WdT[idx] (xin NULL: out = y).
+cudaError_t tc_ffn(const pi_ffn_t *h, int layer, int B, const int32_t *idx, const int32_t *count, const float *xin,
+                   float *out, cudaStream_t s)
+{
+    const pi_ffn_desc_t &D = h->desc;
+    const pi_layer_weights_t &w = h->layers[layer];
+    const int nb = tc_nb(B);
+    const bool pdl = !h->prof;
+    cudaError_t e;
+    {
+        TcArgs a = tc_args();
+        a.w0 = (const uint16_t *)w.w_gate;
+        a.w1 = (const uint16_t *)w.w_up;
+        a.idx = idx;
+        a.count = count;
+        a.f = D.f;
+        a.K = D.d;
+        a.d = D.d;
+        a.xhi = h->tc_uhi;
+        a.xlo = h->tc_ulo;
+        a.ldx = D.d;
+        a.B = B;
+        a.bias = w.b_gate;
+        a.ohi = h->tc_hhi;
+        a.olo = h->tc_hlo;
+        a.ldo = h->tc_fpad;
+        ProfScope p(h, s, PI_K_FFN_H);
+        e = tc_launch(h, D.kind == PI_FFN_GATED_RELU ? TC_GATED : TC_RELU, nb, a, s, pdl);
+    }
+    if (e != cudaSuccess) return e;
+    TcArgs a = tc_args();
+    a.w0 = (const uint16_t *)w.w_down_t;
+    a.idx = idx;
+    a.count = count;
+    a.f = D.f;
+    a.d = D.d;
+    a.xhi = h->tc_hhi;
+    a.xlo = h->tc_hlo;
+    a.ldx = h->tc_fpad;
+    a.B = B;
+    a.xin = xin;
+    a.out = out;
+    ProfScope p(h, s, PI_K_FFN_DOWN);
+    return tc_launch(h, TC_DOWN, nb, a, s, pdl);
+}
+
+cudaError_t enqueue_stack_tc(const pi_ffn_t *h, const float *x0, int B, float *x_out, int32_t *counts,
+                             int32_t *idx_out, cudaStream_t s)
+{
+    const pi_ffn_desc_t &D = h->desc;
+    cudaError_t e;
+    for (int l = 0; l < D.n_layers; ++l) {
+        const float *xl = l == 0 ? x0 : h->xbuf[(l - 1) & 1];
+        float *xn = l == D.n_layers - 1 ? x_out : h->xbuf[l & 1];
+        int32_t *idx = idx_out ? idx_out + (size_t)l * D.f : h->idx_ws;
+        int32_t *cnt = counts ? counts + l : h->counts_ws + l;
+        if ((e = tc_split(h, xl, B, 1, s, l > 0)) != cudaSuccess) return e;
+        if ((e = tc_predict(h, l, B, idx, cnt, s)) != cudaSuccess) return e;
+        if ((e = tc_ffn(h, l, B, idx, cnt, xl, xn, s)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t enqueue_stack(const pi_ffn_t *h, const float *x0, int B, float *x_out, int32_t *counts,
                           int32_t *idx_out, cudaStream_t s)
 {
     const pi_ffn_desc_t &D = h->desc;
+    if (tc_use(h, B)) return enqueue_stack_tc(h, x0, B, x_out, counts, idx_out, s);
     cudaError_t e;
     {
         ProfScope p(h, s, PI_K_RMS);
@@ -447,8 +642,10 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
         }
     }
 
+    plan_tc(h);
     const pi_ffn_desc_t &D = h->desc;
     const size_t mb = (size_t)D.max_batch;
+    const size_t tnb = h->tc_ok ? (size_t)h->tc_nbmax : 0;
     const size_t nred = (size_t)(D.d + RED_COLS - 1) / RED_COLS;
     const size_t sizes[] = {
         mb * D.d * 4, mb * D.d * 4,                    // xbuf[2]
@@ -466,9 +663,14 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
         (size_t)D.n_layers * sizeof(StackLayer),       // stack_layers
         (size_t)D.n_layers * ((D.f + 31) / 32) * 4,    // stack_mask
         (size_t)(D.d + STACK_SLICE - 1) / STACK_SLICE * 4,  // stack_sumsq
+        tnb * D.d * 2, tnb * D.d * 2,                  // tc_uhi, tc_ulo
+        tnb * h->tc_rpad * 2, tnb * h->tc_rpad * 2,    // tc_hphi, tc_hplo
+        tnb * h->tc_fpad * 2, tnb * h->tc_fpad * 2,    // tc_hhi, tc_hlo
+        (size_t)h->nsm * 2 * (2 * tnb) * 128 * 4,      // tc_part
+        h->tc_ok ? (size_t)(h->tc_ntiles + 1) * 4 : 0, // tc_cnt
     };
     const int nbuf = sizeof(sizes) / sizeof(sizes[0]);
-    size_t off[16], total = 0;
+    size_t off[32], total = 0;
     for (int i = 0; i < nbuf; ++i) {
         off[i] = total;
         total = align_up(total + sizes[i], 256);
@@ -499,6 +701,16 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
     h->stack_layers = (StackLayer *)(base + off[13]);
     h->stack_mask = (uint32_t *)(base + off[14]);
     h->stack_sumsq = (float *)(base + off[15]);
+    if (h->tc_ok) {
+        h->tc_uhi = (uint16_t *)(base + off[16]);
+        h->tc_ulo = (uint16_t *)(base + off[17]);
+        h->tc_hphi = (uint16_t *)(base + off[18]);
+        h->tc_hplo = (uint16_t *)(base + off[19]);
+        h->tc_hhi = (uint16_t *)(base + off[20]);
+        h->tc_hlo = (uint16_t *)(base + off[21]);
+        h->tc_part = (float *)(base + off[22]);
+        h->tc_cnt = (uint32_t *)(base + off[23]);
+    }
     {
         std::vector<StackLayer> sl(D.n_layers);
         for (int l = 0; l < D.n_layers; ++l) {
@@ -538,6 +750,11 @@ pi_status_t pi_predict(pi_ffn_t *h, int32_t layer, const float *u, int32_t B, in
     if ((s = check_ptr(u, (size_t)B * D.d * 4, 16, h->dev))) return s;
     if ((s = check_ptr(idx, (size_t)D.f * 4, 4, h->dev))) return s;
     if ((s = check_ptr(count, 4, 4, h->dev))) return s;
+    if (tc_use(h, B)) {
+        cudaError_t e = tc_split(h, u, B, 0, (cudaStream_t)stream, false);
+        if (e == cudaSuccess) e = tc_predict(h, layer, B, idx, count, (cudaStream_t)stream);
+        return cuda_status(e);
+    }
     return cuda_status(enqueue_predict(h, layer, u, nullptr, B, idx, count, (cudaStream_t)stream, false));
 }
 
@@ -551,6 +768,11 @@ pi_status_t pi_sparse_ffn(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
     if ((s = check_ptr(idx, 4, 4, h->dev))) return s;      // length is *count, checked on the device
     if ((s = check_ptr(count, 4, 4, h->dev))) return s;
     if ((s = check_ptr(y, (size_t)B * D.d * 4, 16, h->dev))) return s;
+    if (tc_use(h, B)) {
+        cudaError_t e = tc_split(h, u, B, 0, (cudaStream_t)stream, false);
+        if (e == cudaSuccess) e = tc_ffn(h, layer, B, idx, count, nullptr, y, (cudaStream_t)stream);
+        return cuda_status(e);
+    }
     return cuda_status(enqueue_ffn(h, layer, u, nullptr, B, idx, count, nullptr, y, (cudaStream_t)stream, false));
 }
 
@@ -654,6 +876,10 @@ pi_status_t pi_get_status(pi_ffn_t *h)
     if (v && cudaMemset(h->status, 0, 4) != cudaSuccess) return cuda_status(cudaGetLastError());
     // a grid barrier that gave up leaves its arrival count behind: start the next step clean
     if (v == PI_ERR_TIMEOUT && cudaMemset(h->tickets + 2, 0, 8) != cudaSuccess) return cuda_status(cudaGetLastError());
+    // so does a tensor-core kernel that gave up between its tile tickets
+    if (v == PI_ERR_TIMEOUT && h->tc_cnt &&
+        cudaMemset(h->tc_cnt, 0, (size_t)(h->tc_ntiles + 1) * 4) != cudaSuccess)
+        return cuda_status(cudaGetLastError());
     return (pi_status_t)v;
 }
 

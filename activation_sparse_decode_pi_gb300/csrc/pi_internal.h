@@ -61,6 +61,43 @@ extern template cudaError_t launch_stack_wt<1>(int, int, const StackArgs &, int,
 extern template cudaError_t launch_stack_wt<2>(int, int, const StackArgs &, int, size_t, cudaStream_t);
 extern template cudaError_t launch_stack_wt<3>(int, int, const StackArgs &, int, size_t, cudaStream_t);
 
+// Tensor-core path (batch >= 16): modes of the one kernel template k_tc.
+constexpr int TC_PRED_HIDDEN = 0, TC_LOGITS = 1, TC_GATED = 2, TC_RELU = 3, TC_DOWN = 4;
+constexpr int TC_MAX_STAGES = 8;
+
+struct TcArgs {
+    const uint16_t *w0, *w1;      // weight rows [.. x K] (w1: up rows, gated only); TC_DOWN: W_down^T [f x d]
+    const int32_t *idx, *count;   // gathered row list and its device count (NULL, NULL: rows 0..n_static-1)
+    int n_static;
+    int f;                        // row ids must lie in [0, f)
+    int K, d;                     // contraction length (row modes); model width (TC_DOWN)
+    const uint16_t *xhi, *xlo;    // activations hi/lo [NB x ldx], rows >= B zero
+    int ldx, B;
+    const float *bias;            // per-row bias indexed by row id, or NULL
+    float tau;
+    uint16_t *ohi, *olo;          // outputs hi/lo [NB x ldo] (hidden / h)
+    int ldo;
+    uint32_t *maskw;              // TC_LOGITS: mask words, then ascending idx_out, count_out
+    int32_t *idx_out, *count_out;
+    const float *xin;             // TC_DOWN: residual input or NULL
+    float *out;                   // TC_DOWN: [B x d]
+    float *part;                  // stream-K partials [grid x 2 x ACC x 128]
+    uint32_t *tile_cnt, *done_cnt, *status;   // counters zero on entry, left zero
+    int stages;
+};
+
+template <int WT>
+cudaError_t launch_tc_wt(int mode, int nb, const TcArgs &a, int grid, size_t smem, cudaStream_t s, bool pdl);
+template <int WT>
+cudaError_t launch_tc_split_wt(const float *x, int d, int B, int nb, int ld, int rms, float eps, uint16_t *hi,
+                               uint16_t *lo, cudaStream_t s, bool pdl);
+extern template cudaError_t launch_tc_wt<1>(int, int, const TcArgs &, int, size_t, cudaStream_t, bool);
+extern template cudaError_t launch_tc_wt<2>(int, int, const TcArgs &, int, size_t, cudaStream_t, bool);
+extern template cudaError_t launch_tc_split_wt<1>(const float *, int, int, int, int, int, float, uint16_t *,
+                                                  uint16_t *, cudaStream_t, bool);
+extern template cudaError_t launch_tc_split_wt<2>(const float *, int, int, int, int, int, float, uint16_t *,
+                                                  uint16_t *, cudaStream_t, bool);
+
 struct Launch {
     dim3 grid, block;     // grid.x == 0: persistent grid, one wave of resident CTAs over nsm SMs
     size_t smem;

@@ -1,0 +1,571 @@
+// pi_tc.cuh -- the batch >= 16 path of the sparse FFN on the 5th-generation tensor cores.
+//
+// "PowerInfer" summary page, Methodology: neuron-aware sparse operators touch only the
+// rows of the neurons the predictor marked. With 16 or more sequences decoded together
+// the gathered rows meet enough activation columns to make each one a real contraction:
+//
+//   TC_PRED_HIDDEN  hp  = ReLU(U . P1T^T)             rows of P1T,  K = d
+//   TC_LOGITS       z   = hp . P2T^T + b_p; mask; idx rows of P2T,  K = r
+//   TC_GATED        h   = ReLU(U . Wg^T + bg) * (U . Wu^T)  rows Wg/Wu[idx], K = d
+//   TC_RELU         h   = ReLU(U . W1^T + b1)               rows W1[idx],    K = d
+//   TC_DOWN         y   = H . WdT[idx]  (+ residual)        columns of d, K = active neurons
+//
+// Every product is D[128 x NB] = A[128 x K] * X[NB x K]^T with fp32 accumulation in
+// tensor memory: A is 128 gathered weight rows (K-major) or, for TC_DOWN, a 128-column
+// slice of 64 gathered W_down^T rows per step (MN-major); X is the activation tile,
+// batch rows padded to NB with zeros. The activations are fp32 on the path; they enter
+// the tensor core as the weights' 16-bit type split into hi + lo, two products per step,
+// so the result keeps ~24 bits of the activation, not 8 or 11.
+//
+// Work split (stream-K): the T = tiles x k-blocks iterations are cut into one equal
+// contiguous range per CTA. A tile finished inside one CTA is written out directly; a
+// tile shared by several CTAs leaves fp32 partials, and the CTA whose share completes
+// the tile's k-block count adds them in CTA order, so the result does not depend on
+// timing (only on the grid size).
+//
+// Roles: warps 0-3 drain the accumulators (TMEM lane quarter = warp), warps 4-7 copy
+// the operands into a shared-memory ring with cp.async (16 bytes a thread, swizzled
+// into the 128-byte canonical layouts), warp 8 owns TMEM and one of its threads issues
+// the MMAs. Accumulators are double-buffered so the drain overlaps the next tile.
+// Every wait is bounded (200 ms): on expiry the kernel records PI_ERR_TIMEOUT, stops,
+// waits for its own copies and products, frees its TMEM and returns.
+#pragma once
+
+#include "pi_internal.h"
+#include "pi_umma.cuh"
+
+namespace pi {
+
+constexpr int TC_THREADS = 288;
+
+__host__ __device__ constexpr uint32_t tc_tmem_cols(uint32_t need)
+{
+    return need <= 32 ? 32u : need <= 64 ? 64u : need <= 128 ? 128u : need <= 256 ? 256u : 512u;
+}
+
+__host__ __device__ constexpr uint32_t tc_stage_bytes(int mode, int nb)
+{
+    return (mode == TC_GATED ? 2u : 1u) * 16384u + 2u * (uint32_t)nb * 128u;
+}
+
+// first iteration of CTA c's stream-K range
+__device__ __forceinline__ long long tc_begin(int c, long long T, int P) { return (long long)c * T / P; }
+// CTA whose range holds iteration `it`
+__device__ __forceinline__ int tc_owner(long long it, long long T, int P)
+{
+    return (int)(((it + 1) * P + T - 1) / T - 1);
+}
+
+__device__ __forceinline__ void cp_async_wait_n(int n)
+{
+    switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    default: cp_async_wait<3>(); break;
+    }
+}
+
+// Ascending compaction of the mask words by the 128 drain threads (named barrier 1).
+__device__ __forceinline__ void tc_compact(const uint32_t *__restrict__ maskw, int nwords, int32_t *__restrict__ idx,
+                                           int32_t *__restrict__ count, int *wsum)
+{
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int per = (nwords + 127) / 128;
+    const int w0 = min(nwords, t * per), w1 = min(nwords, w0 + per);
+    int mine = 0;
+    for (int i = w0; i < w1; ++i) mine += __popc(__ldcg(maskw + i));
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    named_sync(1, 128);
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        before += w < warp ? wsum[w] : 0;
+        total += wsum[w];
+    }
+    int off = before + incl - mine;
+    for (int i = w0; i < w1; ++i) {
+        uint32_t m = __ldcg(maskw + i);
+        while (m) {
+            const int bit = __ffs(m) - 1;
+            idx[off++] = i * 32 + bit;
+            m &= m - 1;
+        }
+    }
+    if (t == 0) *count = total;
+    named_sync(1, 128);
+}
+
+template <int WT, int MODE, int NB>
+__global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
+{
+    constexpr bool DOWN = MODE == TC_DOWN;
+    constexpr int NMAT = MODE == TC_GATED ? 2 : 1;
+    constexpr uint32_t A_BYTES = 16384u, X_BYTES = (uint32_t)NB * 128u;
+    constexpr uint32_t STAGE = tc_stage_bytes(MODE, NB);
+    constexpr uint32_t ACC = (uint32_t)(NMAT * NB);
+    constexpr uint32_t TCOLS = tc_tmem_cols(2 * ACC);
+    constexpr uint32_t IDESC = f16_idesc(WT == DT_BF16 ? 1 : 0, DOWN ? 1 : 0, 0, 128, NB);
+    static_assert(NB % 16 == 0 && NB >= 16 && NB <= 128, "batch tile");
+
+    extern __shared__ uint8_t dsm[];
+    __shared__ uint64_t full[TC_MAX_STAGES], empty[TC_MAX_STAGES], accf[2], acce[2], fin;
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int s_abort;    // any role gave up: the others stop early
+    __shared__ volatile int s_dabort;   // written by drain threads only, read after a drain barrier
+    __shared__ int s_last, s_wsum[4];
+
+    const uint32_t sbase = (smem_u32(dsm) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = a.stages;
+    const int LAG = S - 1 < 3 ? S - 1 : 3;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&accf[s], 1);
+            mbar_init(&acce[s], 4);
+        }
+        mbar_init(&fin, 1);
+        s_abort = 0;
+        s_dabort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 8) tmem_alloc(&tmem_base, TCOLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // ---- problem size and this CTA's stream-K range
+    int n = a.n_static;
+    if (a.count) {
+        n = __ldcg(a.count);
+        if (n < 0 || n > a.f) {
+            if (threadIdx.x == 0) set_status(a.status, ST_DEVICE_CHECK);
+            n = n < 0 ? 0 : a.f;
+        }
+    }
+    const int tiles = DOWN ? a.d / 128 : (n + 127) / 128;
+    const int KB = DOWN ? (n + 63) / 64 : a.K / 64;
+    const long long T = (long long)tiles * KB;
+    const int P = gridDim.x, cta = blockIdx.x;
+    const long long it0 = T ? tc_begin(cta, T, P) : 0, it1 = T ? tc_begin(cta + 1, T, P) : 0;
+
+    if (DOWN && n == 0) {   // no active neuron: y = 0
+        for (int e = cta * TC_THREADS + threadIdx.x; e < a.B * a.d; e += P * TC_THREADS)
+            a.out[e] = a.xin ? __ldcg(a.xin + e) : 0.f;
+    }
+
+    if (warp >= 4 && warp < 8) {
+        // ================================================================ producers
+        const int p = threadIdx.x - 128;
+        const uint16_t *const W0 = a.w0;
+        uint32_t q = 0;
+        bool bad = false;
+        if constexpr (!DOWN) {
+            const int prow = p >> 3, pch = p & 7;
+            const uint16_t *rp[NMAT][8];
+            for (long long it = it0; it < it1 && !s_abort;) {
+                const int t = (int)(it / KB), kb0 = (int)(it - (long long)t * KB);
+                const int kb1 = (int)min((long long)KB, kb0 + (it1 - it));
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int j = t * 128 + prow + 16 * i;
+                    int id = -1;
+                    if (j < n) {
+                        id = a.idx ? __ldcg(a.idx + j) : j;
+                        if (id < 0 || id >= a.f) {
+                            bad = true;
+                            id = -1;
+                        }
+                    }
+                    rp[0][i] = id >= 0 ? W0 + (size_t)id * a.K : nullptr;
+                    if constexpr (NMAT == 2) rp[1][i] = id >= 0 ? a.w1 + (size_t)id * a.K : nullptr;
+                }
+                for (int kb = kb0; kb < kb1; ++kb, ++q) {
+                    const int slot = (int)(q % (uint32_t)S);
+                    if (q >= (uint32_t)S && !mbar_wait(&empty[slot], ((q / S) - 1) & 1)) {
+                        set_status(a.status, ST_TIMEOUT);
+                        s_abort = 1;
+                        break;
+                    }
+                    const uint32_t st = sbase + (uint32_t)slot * STAGE;
+#pragma unroll
+                    for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint16_t *src = rp[m][i];
+                            cp_async16(st + m * A_BYTES + sw128_off(prow + 16 * i, pch),
+                                       src ? src + kb * 64 + pch * 8 : W0, src ? 16u : 0u);
+                        }
+                    const uint32_t xs = st + NMAT * A_BYTES;
+#pragma unroll
+                    for (int i = 0; i < NB / 16; ++i) {
+                        const int xb = prow + 16 * i;
+                        const size_t go = (size_t)xb * a.ldx + kb * 64 + pch * 8;
+                        cp_async16(xs + sw128_off(xb, pch), a.xhi + go, 16u);
+                        cp_async16(xs + X_BYTES + sw128_off(xb, pch), a.xlo + go, 16u);
+                    }
+                    cp_async_commit();
+                    if (q >= (uint32_t)LAG) {
+                        cp_async_wait_n(LAG);
+                        fence_proxy_async_smem();
+                        mbar_arrive(&full[(q - LAG) % S]);
+                    }
+                }
+                it += kb1 - kb0;
+            }
+        } else {
+            // W_down^T slice: 64 neuron rows x 128 columns per step; 16 threads a row
+            const int prow = p >> 4, pch = p & 15;
+            const int xrow = p >> 3, xch = p & 7;
+            int ids[8];   // the step's neuron ids; -2 marks the zero rows past the list's end
+            auto load_ids = [&](long long it) {
+                const int kb = (int)(it % KB);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int j = kb * 64 + prow + 8 * i;
+                    ids[i] = j < n ? __ldcg(a.idx + j) : -2;
+                }
+            };
+            if (it0 < it1) load_ids(it0);
+            for (long long it = it0; it < it1 && !s_abort; ++it, ++q) {
+                const int t = (int)(it / KB), kb = (int)(it - (long long)t * KB);
+                const int slot = (int)(q % (uint32_t)S);
+                if (q >= (uint32_t)S && !mbar_wait(&empty[slot], ((q / S) - 1) & 1)) {
+                    set_status(a.status, ST_TIMEOUT);
+                    s_abort = 1;
+                    break;
+                }
+                const uint32_t st = sbase + (uint32_t)slot * STAGE;
+                const size_t col = (size_t)t * 128 + pch * 8;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    int id = ids[i];
+                    if (id >= a.f || id < -2 || id == -1) {
+                        bad = true;
+                        id = -2;
+                    }
+                    cp_async16(st + (uint32_t)(pch >> 3) * 8192u + sw128_off(prow + 8 * i, pch & 7),
+                               id >= 0 ? W0 + (size_t)id * a.d + col : W0, id >= 0 ? 16u : 0u);
+                }
+                const uint32_t xs = st + A_BYTES;
+#pragma unroll
+                for (int i = 0; i < NB / 16; ++i) {
+                    const int xb = xrow + 16 * i;
+                    const size_t go = (size_t)xb * a.ldx + kb * 64 + xch * 8;
+                    cp_async16(xs + sw128_off(xb, xch), a.xhi + go, 16u);
+                    cp_async16(xs + X_BYTES + sw128_off(xb, xch), a.xlo + go, 16u);
+                }
+                cp_async_commit();
+                if (it + 1 < it1) load_ids(it + 1);   // consumed next step: the load overlaps
+                if (q >= (uint32_t)LAG) {
+                    cp_async_wait_n(LAG);
+                    fence_proxy_async_smem();
+                    mbar_arrive(&full[(q - LAG) % S]);
+                }
+            }
+        }
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        for (uint32_t k = q > (uint32_t)LAG ? q - LAG : 0; k < q; ++k) mbar_arrive(&full[k % S]);
+        if (bad) set_status(a.status, ST_DEVICE_CHECK);
+    } else if (warp == 8) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            uint32_t q = 0, si = 0;
+            for (long long it = it0; it < it1 && !s_abort; ++si) {
+                const int t = (int)(it / KB), kb0 = (int)(it - (long long)t * KB);
+                const int kb1 = (int)min((long long)KB, kb0 + (it1 - it));
+                const uint32_t ab = si & 1;
+                if (si >= 2 && !mbar_wait(&acce[ab], ((si >> 1) - 1) & 1)) {
+                    set_status(a.status, ST_TIMEOUT);
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d0 = tmem + ab * ACC;
+                for (int kb = kb0; kb < kb1; ++kb, ++q) {
+                    const int slot = (int)(q % (uint32_t)S);
+                    if (!mbar_wait(&full[slot], (q / S) & 1)) {
+                        set_status(a.status, ST_TIMEOUT);
+                        s_abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = sbase + (uint32_t)slot * STAGE;
+                    const uint32_t xh = st + NMAT * A_BYTES, xl = xh + X_BYTES;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint64_t bh = sw128_desc(xh + j * 32, 16, 1024), bl = sw128_desc(xl + j * 32, 16, 1024);
+#pragma unroll
+                        for (int m = 0; m < NMAT; ++m) {
+                            const uint64_t ad = DOWN ? sw128_desc(st + j * 2048, 8192, 1024)
+                                                     : sw128_desc(st + m * A_BYTES + j * 32, 16, 1024);
+                            umma_f16(d0 + m * NB, ad, bh, IDESC, kb > kb0 || j > 0);
+                            umma_f16(d0 + m * NB, ad, bl, IDESC, true);
+                        }
+                    }
+                    umma_commit(&empty[slot]);
+                }
+                if (s_abort) break;
+                umma_commit(&accf[ab]);
+                it += kb1 - kb0;
+            }
+            umma_commit(&fin);
+            if (!mbar_wait(&fin, 0)) set_status(a.status, ST_TIMEOUT);
+        }
+    } else {
+        // ================================================================ drain (warps 0-3)
+        const int m = 32 * warp + lane;
+        const int nwords = (a.f + 31) / 32;
+        uint32_t si = 0;
+        for (long long it = it0; it < it1; ++si) {
+            const int t = (int)(it / KB), kb0 = (int)(it - (long long)t * KB);
+            const int kb1 = (int)min((long long)KB, kb0 + (it1 - it));
+            it += kb1 - kb0;
+            const uint32_t ab = si & 1;
+            // all four drain warps take the same decision, so none is left at a named barrier
+            if (!mbar_wait(&accf[ab], (si >> 1) & 1)) s_dabort = 1;
+            named_sync(1, 128);
+            if (s_dabort) {
+                if (threadIdx.x == 0) set_status(a.status, ST_TIMEOUT);
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(32 * warp) << 16) + ab * ACC;
+            const bool whole = kb0 == 0 && kb1 == KB;
+            float *mypart = nullptr;
+            if (!whole) {
+                const int slot = it0 >= (long long)t * KB ? 0 : 1;
+                mypart = a.part + (size_t)(cta * 2 + slot) * ACC * 128;
+                for (uint32_t c = 0; c < ACC; c += 16) {
+                    float v[16];
+                    tmem_ld16(tb + c, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) mypart[(c + i) * 128 + m] = v[i];
+                }
+            }
+            // the tile's final values, 16 batch columns at a time, from TMEM or from the partials
+            auto chunk = [&](int c, float (&v)[NMAT][16]) {
+                if (whole) {
+#pragma unroll
+                    for (int mm = 0; mm < NMAT; ++mm) tmem_ld16(tb + mm * NB + c, v[mm]);
+                } else {
+#pragma unroll
+                    for (int mm = 0; mm < NMAT; ++mm)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[mm][i] = 0.f;
+                    const long long tb0 = (long long)t * KB, te = tb0 + KB - 1;
+                    const int c0 = tc_owner(tb0, T, P), c1 = tc_owner(te, T, P);
+                    for (int cc = c0; cc <= c1; ++cc) {
+                        const long long b0 = tc_begin(cc, T, P);
+                        if (tc_begin(cc + 1, T, P) == b0) continue;   // empty range
+                        const float *pp = a.part + (size_t)(cc * 2 + (b0 >= tb0 ? 0 : 1)) * ACC * 128;
+#pragma unroll
+                        for (int mm = 0; mm < NMAT; ++mm)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[mm][i] += __ldcg(pp + (mm * NB + c + i) * 128 + m);
+                    }
+                }
+            };
+            bool last = whole;
+            if (!whole) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acce[ab]);
+                named_sync(1, 128);
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    const int add = kb1 - kb0;
+                    const unsigned old = atomicAdd(a.tile_cnt + t, (unsigned)add);
+                    s_last = (int)old + add == KB;
+                }
+                named_sync(1, 128);
+                last = s_last != 0;
+                if (last) __threadfence();
+            }
+            if (last) {
+                const int j = t * 128 + m;   // output row of the tile (DOWN: column of d)
+                int id = -1;
+                if constexpr (!DOWN) {
+                    if (j < n) {
+                        id = a.idx ? __ldcg(a.idx + j) : j;
+                        if (id < 0 || id >= a.f) id = -1;
+                    }
+                }
+                const float bias = (id >= 0 && a.bias) ? __ldg(a.bias + id) : 0.f;
+                bool act = false;
+                for (int c = 0; c < NB; c += 16) {
+                    float v[NMAT][16];
+                    chunk(c, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int b = c + i;
+                        if constexpr (DOWN) {
+                            if (b < a.B) {
+                                const size_t o = (size_t)b * a.d + j;
+                                a.out[o] = (a.xin ? __ldcg(a.xin + o) : 0.f) + v[0][i];
+                            }
+                        } else if constexpr (MODE == TC_LOGITS) {
+                            act |= id >= 0 && b < a.B && (v[0][i] + bias > a.tau);
+                        } else {
+                            float hv = 0.f;
+                            if (b < a.B && id >= 0) {
+                                if constexpr (MODE == TC_PRED_HIDDEN) hv = fmaxf(v[0][i], 0.f);
+                                else if constexpr (MODE == TC_RELU) hv = fmaxf(v[0][i] + bias, 0.f);
+                                else hv = fmaxf(v[0][i] + bias, 0.f) * v[1][i];
+                            }
+                            if (j < a.ldo) {
+                                uint16_t hi, lo;
+                                split16<WT>(hv, hi, lo);
+                                a.ohi[(size_t)b * a.ldo + j] = hi;
+                                a.olo[(size_t)b * a.ldo + j] = lo;
+                            }
+                        }
+                    }
+                }
+                if (whole) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acce[ab]);
+                } else if (threadIdx.x == 0) {
+                    a.tile_cnt[t] = 0u;
+                }
+                if constexpr (MODE == TC_LOGITS) {
+                    const uint32_t word = __ballot_sync(0xffffffffu, act);
+                    const int wi = (t * 128 + 32 * warp) >> 5;
+                    if (lane == 0 && wi < nwords) a.maskw[wi] = word;
+                    named_sync(1, 128);
+                    if (threadIdx.x == 0) {
+                        __threadfence();
+                        s_last = atomicAdd(a.done_cnt, 1u) == (unsigned)tiles - 1;
+                    }
+                    named_sync(1, 128);
+                    if (s_last) {
+                        __threadfence();
+                        tc_compact(a.maskw, nwords, a.idx_out, a.count_out, s_wsum);
+                        if (threadIdx.x == 0) *a.done_cnt = 0u;
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown: all copies and products of this CTA are complete
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TCOLS);
+    }
+}
+
+// x [B x d] fp32 -> hi, lo [NB x ld] in the weights' 16-bit type; rows B..NB-1 zero.
+// rms: scale row b by 1/sqrt(mean(x_b^2) + eps) first (the stack's pre-norm).
+template <int WT>
+__global__ void __launch_bounds__(256) k_tc_split(const float *__restrict__ x, int d, int B, int ld, int rms, float eps,
+                                                  uint16_t *__restrict__ hi, uint16_t *__restrict__ lo)
+{
+    __shared__ float ws[8];
+    const int b = blockIdx.x;
+    pdl_launch_dependents();
+    pdl_wait();
+    uint2 *h2 = reinterpret_cast<uint2 *>(hi + (size_t)b * ld), *l2 = reinterpret_cast<uint2 *>(lo + (size_t)b * ld);
+    if (b >= B) {
+        for (int i = threadIdx.x; i < d / 4; i += blockDim.x) h2[i] = l2[i] = make_uint2(0u, 0u);
+        return;
+    }
+    const float4 *x4 = reinterpret_cast<const float4 *>(x + (size_t)b * d);
+    float inv = 1.f;
+    if (rms) {
+        float t = 0.f;
+        for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+            const float4 v = __ldcg(x4 + i);
+            t = fmaf(v.x, v.x, t);
+            t = fmaf(v.y, v.y, t);
+            t = fmaf(v.z, v.z, t);
+            t = fmaf(v.w, v.w, t);
+        }
+        t = warp_sum(t);
+        if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = t;
+        __syncthreads();
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += ws[w];
+        inv = 1.0f / sqrtf(s / (float)d + eps);
+    }
+    for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+        const float4 v = __ldcg(x4 + i);
+        const float e[4] = {v.x * inv, v.y * inv, v.z * inv, v.w * inv};
+        uint16_t hh[4], ll[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) split16<WT>(e[k], hh[k], ll[k]);
+        h2[i] = make_uint2(hh[0] | ((uint32_t)hh[1] << 16), hh[2] | ((uint32_t)hh[3] << 16));
+        l2[i] = make_uint2(ll[0] | ((uint32_t)ll[1] << 16), ll[2] | ((uint32_t)ll[3] << 16));
+    }
+}
+
+template <int WT>
+cudaError_t launch_tc_wt(int mode, int nb, const TcArgs &a, int grid, size_t smem, cudaStream_t s, bool pdl)
+{
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = ensure_smem(kern, smem);
+        if (e != cudaSuccess) return e;
+        Launch L;
+        L.grid = dim3(grid);
+        L.block = dim3(TC_THREADS);
+        L.smem = smem;
+        L.stream = s;
+        L.pdl = pdl;
+        L.nsm = grid;
+        return launch_ex(L, kern, a);
+    };
+#define PI_TC_NB(MODE)                                   \
+    switch (nb) {                                        \
+    case 16: return go(k_tc<WT, MODE, 16>);              \
+    case 32: return go(k_tc<WT, MODE, 32>);              \
+    case 64: return go(k_tc<WT, MODE, 64>);              \
+    case 128: return go(k_tc<WT, MODE, 128>);            \
+    }                                                    \
+    break;
+    switch (mode) {
+    case TC_PRED_HIDDEN: PI_TC_NB(TC_PRED_HIDDEN)
+    case TC_LOGITS: PI_TC_NB(TC_LOGITS)
+    case TC_GATED: PI_TC_NB(TC_GATED)
+    case TC_RELU: PI_TC_NB(TC_RELU)
+    case TC_DOWN: PI_TC_NB(TC_DOWN)
+    }
+#undef PI_TC_NB
+    return cudaErrorInvalidValue;
+}
+
+template <int WT>
+cudaError_t launch_tc_split_wt(const float *x, int d, int B, int nb, int ld, int rms, float eps, uint16_t *hi,
+                               uint16_t *lo, cudaStream_t s, bool pdl)
+{
+    Launch L;
+    L.grid = dim3(nb);
+    L.block = dim3(256);
+    L.smem = 0;
+    L.stream = s;
+    L.pdl = pdl;
+    L.nsm = nb;
+    return launch_ex(L, k_tc_split<WT>, x, d, B, ld, rms, eps, hi, lo);
+}
+
+}  // namespace pi

@@ -1,0 +1,8 @@
+// pi_tc_f16.cu -- tensor-core batch >= 16 kernels, f16 weights (see pi_tc.cuh).
+#include "pi_tc.cuh"
+
+namespace pi {
+template cudaError_t launch_tc_wt<2>(int, int, const TcArgs &, int, size_t, cudaStream_t, bool);
+template cudaError_t launch_tc_split_wt<2>(const float *, int, int, int, int, int, float, uint16_t *, uint16_t *,
+                                           cudaStream_t, bool);
+}  // namespace pi

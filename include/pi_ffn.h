@@ -228,6 +228,22 @@ pi_status_t pi_sparse_ffn_noalloc(const pi_ffn_desc_t *desc, const pi_layer_weig
  */
 pi_status_t pi_selftest_grid_barrier(uint32_t *work, int32_t extra, void *stream);
 
+/*
+ * Check of the tensor-core (tcgen05) operand layouts used by the batch >= 16 path: one
+ * CTA stages A and B in shared memory the way those kernels do, multiplies them on the
+ * tensor cores with an fp32 accumulator in tensor memory, and writes
+ * d[128 x n] = A * B^T (row-major fp32, device).
+ *   a: device, 16-bit elements of `dtype` (PI_BF16 or PI_F16). mode 0: A as [128 x k]
+ *      row-major (staged K-major). mode 1: A^T as [k x 128] row-major (staged MN-major).
+ *   b: device, [n x k] row-major (staged K-major).
+ *   n in {16, 32, 64, 128}; k in {64, 128}. a, b, d 16-byte aligned.
+ *   status: device uint32, set to PI_ERR_TIMEOUT if the product's completion is not
+ *   signalled within 200 ms (the kernel then returns without writing d).
+ * Returns PI_ERR_INVALID_ARG for other shapes or non-device pointers.
+ */
+pi_status_t pi_selftest_umma(const void *a, const void *b, float *d, int32_t mode, int32_t n, int32_t k,
+                             int32_t dtype, uint32_t *status, void *stream);
+
 /* Wait for all work on the device, return the first kernel-recorded error and clear it. */
 pi_status_t pi_get_status(pi_ffn_t *h);
 
