@@ -139,8 +139,9 @@ struct pi_ffn {
     // tensor-core path (batch >= tc_min_b)
     bool tc_ok = false;
     int tc_min_b = 16, tc_nbmax = 0, tc_rpad = 0, tc_fpad = 0;
-    int tc_stages[5][4] = {};          // [mode][log2(NB / 16)]
-    size_t tc_smem[5][4] = {};
+    int tc_stages[5][4][3] = {};       // [mode][log2(NB / 16)][log2(w)]
+    size_t tc_smem[5][4][3] = {};
+    int tc_kw = 1, tc_ds = 1, tc_stage_cap = TC_MAX_STAGES;   // tuning (PI_FFN_TC_KW / _DS / _STAGES)
     uint16_t *tc_uhi = nullptr, *tc_ulo = nullptr, *tc_hphi = nullptr, *tc_hplo = nullptr, *tc_hhi = nullptr,
              *tc_hlo = nullptr;
     float *tc_part = nullptr;
@@ -311,16 +312,29 @@ void plan_tc(pi_ffn_t *h)
         cudaGetLastError();
         return;
     }
+    auto env_int = [](const char *name, int def) {
+        const char *v = std::getenv(name);
+        return v && std::atoi(v) > 0 ? std::atoi(v) : def;
+    };
+    h->tc_kw = env_int("PI_FFN_TC_KW", 1) >= 2 ? 2 : 1;
+    h->tc_ds = std::min(4, env_int("PI_FFN_TC_DS", 1));
+    if (h->tc_ds == 3) h->tc_ds = 2;
+    h->tc_stage_cap = std::min(TC_MAX_STAGES, env_int("PI_FFN_TC_STAGES", TC_MAX_STAGES));
     const size_t avail = (size_t)optin > 2048 ? (size_t)optin - 2048 : 0;   // alignment slack + static barriers
     for (int mode = 0; mode < 5; ++mode)
-        for (int i = 0; i < 4; ++i) {
-            const int nb = 16 << i;
-            const size_t stage = (mode == TC_GATED ? 2 : 1) * 16384 + 2 * (size_t)nb * 128;
-            const int st = (int)std::min<size_t>(TC_MAX_STAGES, avail / stage);
-            if (st < 2) return;
-            h->tc_stages[mode][i] = st;
-            h->tc_smem[mode][i] = 1024 + (size_t)st * stage;
-        }
+        for (int i = 0; i < 4; ++i)
+            for (int wi = 0; wi < 3; ++wi) {
+                const int nb = 16 << i, w = 1 << wi;
+                const size_t stage = mode == TC_DOWN ? (size_t)w * 16384 + 2 * (size_t)nb * 128
+                                                     : (mode == TC_GATED ? 2 : 1) * (size_t)w * 16384 +
+                                                           2 * (size_t)w * nb * 128;
+                const int st = (int)std::min<size_t>((size_t)h->tc_stage_cap, avail / stage);
+                h->tc_stages[mode][i][wi] = st;
+                h->tc_smem[mode][i][wi] = 1024 + (size_t)st * stage;
+            }
+    for (int mode = 0; mode < 5; ++mode)   // every mode must fit with w = 1
+        for (int i = 0; i < 4; ++i)
+            if (h->tc_stages[mode][i][0] < 2) return;
     h->tc_nbmax = tc_nb(std::min(D.max_batch, 128));
     h->tc_rpad = (D.r + 127) / 128 * 128;
     h->tc_fpad = (D.f + 127) / 128 * 128;
@@ -328,17 +342,48 @@ void plan_tc(pi_ffn_t *h)
     h->tc_ok = true;
 }
 
+// Width of one pipeline step (row modes: 64-wide K blocks; TC_DOWN: 128-column slices).
+int tc_width(const pi_ffn_t *h, int mode, int nb, int K)
+{
+    if (mode == TC_DOWN) {
+        int w = h->tc_ds;
+        while (w > 1 && (h->desc.d % (128 * w) || 2 * w * nb > 512)) w /= 2;
+        return w;
+    }
+    return h->tc_kw == 2 && K % 128 == 0 ? 2 : 1;
+}
+
+template <int WT>
+cudaError_t tc_dispatch(int mode, int nb, int w, const TcArgs &a, int grid, size_t smem, cudaStream_t s, bool pdl)
+{
+    switch (mode) {
+    case TC_PRED_HIDDEN: return launch_tc_mode<WT, TC_PRED_HIDDEN>(nb, w, a, grid, smem, s, pdl);
+    case TC_LOGITS: return launch_tc_mode<WT, TC_LOGITS>(nb, w, a, grid, smem, s, pdl);
+    case TC_GATED: return launch_tc_mode<WT, TC_GATED>(nb, w, a, grid, smem, s, pdl);
+    case TC_RELU: return launch_tc_mode<WT, TC_RELU>(nb, w, a, grid, smem, s, pdl);
+    case TC_DOWN: return launch_tc_mode<WT, TC_DOWN>(nb, w, a, grid, smem, s, pdl);
+    }
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t tc_launch(const pi_ffn_t *h, int mode, int nb, const TcArgs &a0, cudaStream_t s, bool pdl)
 {
     TcArgs a = a0;
     const int i = tc_nbi(nb);
-    a.stages = h->tc_stages[mode][i];
+    int w = tc_width(h, mode, nb, a.K);
+    int wi = w == 1 ? 0 : w == 2 ? 1 : 2;
+    if (h->tc_stages[mode][i][wi] < 2) {   // that width does not fit shared memory: one block per step
+        w = 1;
+        wi = 0;
+    }
+    a.stages = h->tc_stages[mode][i][wi];
     a.part = h->tc_part;
     a.tile_cnt = h->tc_cnt;
     a.done_cnt = h->tc_cnt + h->tc_ntiles;
     a.status = h->status;
-    return h->desc.wdtype == PI_BF16 ? launch_tc_wt<1>(mode, nb, a, h->nsm, h->tc_smem[mode][i], s, pdl)
-                                     : launch_tc_wt<2>(mode, nb, a, h->nsm, h->tc_smem[mode][i], s, pdl);
+    const size_t smem = h->tc_smem[mode][i][wi];
+    return h->desc.wdtype == PI_BF16 ? tc_dispatch<1>(mode, nb, w, a, h->nsm, smem, s, pdl)
+                                     : tc_dispatch<2>(mode, nb, w, a, h->nsm, smem, s, pdl);
 }
 
 // u (or x_l with rms) -> uhi, ulo [NB x d]
@@ -666,7 +711,7 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
         tnb * D.d * 2, tnb * D.d * 2,                  // tc_uhi, tc_ulo
         tnb * h->tc_rpad * 2, tnb * h->tc_rpad * 2,    // tc_hphi, tc_hplo
         tnb * h->tc_fpad * 2, tnb * h->tc_fpad * 2,    // tc_hhi, tc_hlo
-        (size_t)h->nsm * 2 * (2 * tnb) * 128 * 4,      // tc_part
+        (size_t)h->nsm * 2 * 256 * 128 * 4 * (tnb ? 1 : 0),   // tc_part: two slots of up to 256 accumulator columns
         h->tc_ok ? (size_t)(h->tc_ntiles + 1) * 4 : 0, // tc_cnt
     };
     const int nbuf = sizeof(sizes) / sizeof(sizes[0]);

@@ -86,13 +86,18 @@ struct TcArgs {
     int stages;
 };
 
-template <int WT>
-cudaError_t launch_tc_wt(int mode, int nb, const TcArgs &a, int grid, size_t smem, cudaStream_t s, bool pdl);
+// w: 64-wide K blocks per pipeline step (row modes: 1, 2), or 128-column slices per
+// W_down^T tile (TC_DOWN: 1, 2, 4 with 2 * w * nb <= 512).
+template <int WT, int MODE>
+cudaError_t launch_tc_mode(int nb, int w, const TcArgs &a, int grid, size_t smem, cudaStream_t s, bool pdl);
+#define PI_TC_EXTERN(WT, MODE) \
+    extern template cudaError_t launch_tc_mode<WT, MODE>(int, int, const TcArgs &, int, size_t, cudaStream_t, bool);
+PI_TC_EXTERN(1, 0) PI_TC_EXTERN(1, 1) PI_TC_EXTERN(1, 2) PI_TC_EXTERN(1, 3) PI_TC_EXTERN(1, 4)
+PI_TC_EXTERN(2, 0) PI_TC_EXTERN(2, 1) PI_TC_EXTERN(2, 2) PI_TC_EXTERN(2, 3) PI_TC_EXTERN(2, 4)
+#undef PI_TC_EXTERN
 template <int WT>
 cudaError_t launch_tc_split_wt(const float *x, int d, int B, int nb, int ld, int rms, float eps, uint16_t *hi,
                                uint16_t *lo, cudaStream_t s, bool pdl);
-extern template cudaError_t launch_tc_wt<1>(int, int, const TcArgs &, int, size_t, cudaStream_t, bool);
-extern template cudaError_t launch_tc_wt<2>(int, int, const TcArgs &, int, size_t, cudaStream_t, bool);
 extern template cudaError_t launch_tc_split_wt<1>(const float *, int, int, int, int, int, float, uint16_t *,
                                                   uint16_t *, cudaStream_t, bool);
 extern template cudaError_t launch_tc_split_wt<2>(const float *, int, int, int, int, int, float, uint16_t *,

@@ -31,6 +31,8 @@
 // waits for its own copies and products, frees its TMEM and returns.
 #pragma once
 
+#include <type_traits>
+
 #include "pi_internal.h"
 #include "pi_umma.cuh"
 
@@ -43,9 +45,11 @@ __host__ __device__ constexpr uint32_t tc_tmem_cols(uint32_t need)
     return need <= 32 ? 32u : need <= 64 ? 64u : need <= 128 ? 128u : need <= 256 ? 256u : 512u;
 }
 
-__host__ __device__ constexpr uint32_t tc_stage_bytes(int mode, int nb)
+// bytes of one pipeline step: weight blocks, then activation hi and lo blocks
+__host__ __device__ constexpr uint32_t tc_stage_bytes(int mode, int nb, int w)
 {
-    return (mode == TC_GATED ? 2u : 1u) * 16384u + 2u * (uint32_t)nb * 128u;
+    return mode == TC_DOWN ? (uint32_t)w * 16384u + 2u * (uint32_t)nb * 128u
+                           : (mode == TC_GATED ? 2u : 1u) * (uint32_t)w * 16384u + 2u * (uint32_t)w * nb * 128u;
 }
 
 // first iteration of CTA c's stream-K range
@@ -62,7 +66,11 @@ __device__ __forceinline__ void cp_async_wait_n(int n)
     case 0: cp_async_wait<0>(); break;
     case 1: cp_async_wait<1>(); break;
     case 2: cp_async_wait<2>(); break;
-    default: cp_async_wait<3>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
     }
 }
 
@@ -102,17 +110,33 @@ __device__ __forceinline__ void tc_compact(const uint32_t *__restrict__ maskw, i
     named_sync(1, 128);
 }
 
-template <int WT, int MODE, int NB>
+// Ticket on a tile counter: release this CTA's partial (written before the caller's
+// CTA-level barrier), and acquire everyone else's when the returned value completes the tile.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// W: 64-wide K blocks per pipeline step (row modes), or 128-column W_down^T slices per tile (TC_DOWN).
+template <int WT, int MODE, int NB, int W>
 __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
 {
     constexpr bool DOWN = MODE == TC_DOWN;
     constexpr int NMAT = MODE == TC_GATED ? 2 : 1;
-    constexpr uint32_t A_BYTES = 16384u, X_BYTES = (uint32_t)NB * 128u;
-    constexpr uint32_t STAGE = tc_stage_bytes(MODE, NB);
-    constexpr uint32_t ACC = (uint32_t)(NMAT * NB);
+    constexpr int NACC = DOWN ? W : NMAT;                  // NB-wide accumulators per tile
+    constexpr int KW = DOWN ? 1 : W;                       // 64-wide K blocks per step
+    constexpr uint32_t BLK = 16384u;                       // one 128 x 64 (or 64 x 128) operand block
+    constexpr uint32_t XB = (uint32_t)NB * 128u;           // one NB x 64 activation block
+    constexpr uint32_t A_BYTES = (uint32_t)(DOWN ? W : NMAT * KW) * BLK;
+    constexpr uint32_t STAGE = tc_stage_bytes(MODE, NB, W);
+    constexpr uint32_t ACC = (uint32_t)(NACC * NB);
     constexpr uint32_t TCOLS = tc_tmem_cols(2 * ACC);
     constexpr uint32_t IDESC = f16_idesc(WT == DT_BF16 ? 1 : 0, DOWN ? 1 : 0, 0, 128, NB);
     static_assert(NB % 16 == 0 && NB >= 16 && NB <= 128, "batch tile");
+    static_assert(2 * ACC <= 512, "accumulators exceed tensor memory");
+    static_assert(A_BYTES + 2u * KW * XB == STAGE, "stage layout");
 
     extern __shared__ uint8_t dsm[];
     __shared__ uint64_t full[TC_MAX_STAGES], empty[TC_MAX_STAGES], accf[2], acce[2], fin;
@@ -124,7 +148,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
     const uint32_t sbase = (smem_u32(dsm) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = a.stages;
-    const int LAG = S - 1 < 3 ? S - 1 : 3;
+    const int LAG = S - 1 < TC_MAX_STAGES - 1 ? S - 1 : TC_MAX_STAGES - 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -158,8 +182,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
             n = n < 0 ? 0 : a.f;
         }
     }
-    const int tiles = DOWN ? a.d / 128 : (n + 127) / 128;
-    const int KB = DOWN ? (n + 63) / 64 : a.K / 64;
+    const int tiles = DOWN ? a.d / (128 * W) : (n + 127) / 128;
+    const int KB = DOWN ? (n + 63) / 64 : a.K / (64 * KW);   // pipeline steps per tile
     const long long T = (long long)tiles * KB;
     const int P = gridDim.x, cta = blockIdx.x;
     const long long it0 = T ? tc_begin(cta, T, P) : 0, it1 = T ? tc_begin(cta + 1, T, P) : 0;
@@ -175,7 +199,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
         const uint16_t *const W0 = a.w0;
         uint32_t q = 0;
         bool bad = false;
+        auto step_done = [&]() {
+            cp_async_commit();
+            if (q >= (uint32_t)LAG) {
+                cp_async_wait_n(LAG);
+                fence_proxy_async_smem();
+                mbar_arrive(&full[(q - LAG) % S]);
+            }
+        };
         if constexpr (!DOWN) {
+            // 128 gathered rows x (KW x 64) columns per step; 8 threads per 128-byte row piece
             const int prow = p >> 3, pch = p & 7;
             const uint16_t *rp[NMAT][8];
             for (long long it = it0; it < it1 && !s_abort;) {
@@ -204,32 +237,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                     }
                     const uint32_t st = sbase + (uint32_t)slot * STAGE;
 #pragma unroll
-                    for (int m = 0; m < NMAT; ++m)
+                    for (int w = 0; w < KW; ++w) {
+                        const int k0 = (kb * KW + w) * 64 + pch * 8;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const uint16_t *src = rp[m][i];
-                            cp_async16(st + m * A_BYTES + sw128_off(prow + 16 * i, pch),
-                                       src ? src + kb * 64 + pch * 8 : W0, src ? 16u : 0u);
+                        for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const uint16_t *src = rp[m][i];
+                                cp_async16(st + (m * KW + w) * BLK + sw128_off(prow + 16 * i, pch), src ? src + k0 : W0,
+                                           src ? 16u : 0u);
+                            }
+                        const uint32_t xs = st + A_BYTES + w * XB;
+#pragma unroll
+                        for (int i = 0; i < NB / 16; ++i) {
+                            const int xb = prow + 16 * i;
+                            const size_t go = (size_t)xb * a.ldx + k0;
+                            cp_async16(xs + sw128_off(xb, pch), a.xhi + go, 16u);
+                            cp_async16(xs + KW * XB + sw128_off(xb, pch), a.xlo + go, 16u);
                         }
-                    const uint32_t xs = st + NMAT * A_BYTES;
-#pragma unroll
-                    for (int i = 0; i < NB / 16; ++i) {
-                        const int xb = prow + 16 * i;
-                        const size_t go = (size_t)xb * a.ldx + kb * 64 + pch * 8;
-                        cp_async16(xs + sw128_off(xb, pch), a.xhi + go, 16u);
-                        cp_async16(xs + X_BYTES + sw128_off(xb, pch), a.xlo + go, 16u);
                     }
-                    cp_async_commit();
-                    if (q >= (uint32_t)LAG) {
-                        cp_async_wait_n(LAG);
-                        fence_proxy_async_smem();
-                        mbar_arrive(&full[(q - LAG) % S]);
-                    }
+                    step_done();
                 }
                 it += kb1 - kb0;
             }
         } else {
-            // W_down^T slice: 64 neuron rows x 128 columns per step; 16 threads a row
+            // W_down^T: 64 neuron rows x (W x 128) columns per step; 16 threads per 256-byte row piece
             const int prow = p >> 4, pch = p & 15;
             const int xrow = p >> 3, xch = p & 7;
             int ids[8];   // the step's neuron ids; -2 marks the zero rows past the list's end
@@ -251,7 +283,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                     break;
                 }
                 const uint32_t st = sbase + (uint32_t)slot * STAGE;
-                const size_t col = (size_t)t * 128 + pch * 8;
+                const uint16_t *src[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     int id = ids[i];
@@ -259,24 +291,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                         bad = true;
                         id = -2;
                     }
-                    cp_async16(st + (uint32_t)(pch >> 3) * 8192u + sw128_off(prow + 8 * i, pch & 7),
-                               id >= 0 ? W0 + (size_t)id * a.d + col : W0, id >= 0 ? 16u : 0u);
+                    src[i] = id >= 0 ? W0 + (size_t)id * a.d + (size_t)t * 128 * W + pch * 8 : nullptr;
                 }
+#pragma unroll
+                for (int w = 0; w < W; ++w)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        cp_async16(st + w * BLK + (uint32_t)(pch >> 3) * 8192u + sw128_off(prow + 8 * i, pch & 7),
+                                   src[i] ? src[i] + w * 128 : W0, src[i] ? 16u : 0u);
                 const uint32_t xs = st + A_BYTES;
 #pragma unroll
                 for (int i = 0; i < NB / 16; ++i) {
                     const int xb = xrow + 16 * i;
                     const size_t go = (size_t)xb * a.ldx + kb * 64 + xch * 8;
                     cp_async16(xs + sw128_off(xb, xch), a.xhi + go, 16u);
-                    cp_async16(xs + X_BYTES + sw128_off(xb, xch), a.xlo + go, 16u);
+                    cp_async16(xs + XB + sw128_off(xb, xch), a.xlo + go, 16u);
                 }
-                cp_async_commit();
                 if (it + 1 < it1) load_ids(it + 1);   // consumed next step: the load overlaps
-                if (q >= (uint32_t)LAG) {
-                    cp_async_wait_n(LAG);
-                    fence_proxy_async_smem();
-                    mbar_arrive(&full[(q - LAG) % S]);
-                }
+                step_done();
             }
         }
         cp_async_wait_all();
@@ -307,16 +339,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                     }
                     tc_fence_after();
                     const uint32_t st = sbase + (uint32_t)slot * STAGE;
-                    const uint32_t xh = st + NMAT * A_BYTES, xl = xh + X_BYTES;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint64_t bh = sw128_desc(xh + j * 32, 16, 1024), bl = sw128_desc(xl + j * 32, 16, 1024);
+                    for (int w = 0; w < KW; ++w) {
+                        const uint32_t xh = st + A_BYTES + w * XB, xl = xh + KW * XB;
 #pragma unroll
-                        for (int m = 0; m < NMAT; ++m) {
-                            const uint64_t ad = DOWN ? sw128_desc(st + j * 2048, 8192, 1024)
-                                                     : sw128_desc(st + m * A_BYTES + j * 32, 16, 1024);
-                            umma_f16(d0 + m * NB, ad, bh, IDESC, kb > kb0 || j > 0);
-                            umma_f16(d0 + m * NB, ad, bl, IDESC, true);
+                        for (int j = 0; j < 4; ++j) {
+                            const uint64_t bh = sw128_desc(xh + j * 32, 16, 1024);
+                            const uint64_t bl = sw128_desc(xl + j * 32, 16, 1024);
+                            const bool acc = kb > kb0 || w > 0 || j > 0;
+#pragma unroll
+                            for (int m = 0; m < NACC; ++m) {
+                                const uint64_t ad = DOWN ? sw128_desc(st + m * BLK + j * 2048, 8192, 1024)
+                                                         : sw128_desc(st + (m * KW + w) * BLK + j * 32, 16, 1024);
+                                umma_f16(d0 + m * NB, ad, bh, IDESC, acc);
+                                umma_f16(d0 + m * NB, ad, bl, IDESC, true);
+                            }
                         }
                     }
                     umma_commit(&empty[slot]);
@@ -349,10 +386,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(32 * warp) << 16) + ab * ACC;
             const bool whole = kb0 == 0 && kb1 == KB;
-            float *mypart = nullptr;
             if (!whole) {
                 const int slot = it0 >= (long long)t * KB ? 0 : 1;
-                mypart = a.part + (size_t)(cta * 2 + slot) * ACC * 128;
+                float *mypart = a.part + (size_t)(cta * 2 + slot) * ACC * 128;
                 for (uint32_t c = 0; c < ACC; c += 16) {
                     float v[16];
                     tmem_ld16(tb + c, v);
@@ -361,26 +397,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                 }
             }
             // the tile's final values, 16 batch columns at a time, from TMEM or from the partials
-            auto chunk = [&](int c, float (&v)[NMAT][16]) {
+            auto chunk = [&](int c, float (&v)[NACC][16]) {
                 if (whole) {
 #pragma unroll
-                    for (int mm = 0; mm < NMAT; ++mm) tmem_ld16(tb + mm * NB + c, v[mm]);
-                } else {
+                    for (int mm = 0; mm < NACC; ++mm) tmem_ld16(tb + mm * NB + c, v[mm]);
+                    return;
+                }
 #pragma unroll
-                    for (int mm = 0; mm < NMAT; ++mm)
+                for (int mm = 0; mm < NACC; ++mm)
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[mm][i] = 0.f;
-                    const long long tb0 = (long long)t * KB, te = tb0 + KB - 1;
-                    const int c0 = tc_owner(tb0, T, P), c1 = tc_owner(te, T, P);
-                    for (int cc = c0; cc <= c1; ++cc) {
-                        const long long b0 = tc_begin(cc, T, P);
-                        if (tc_begin(cc + 1, T, P) == b0) continue;   // empty range
+                    for (int i = 0; i < 16; ++i) v[mm][i] = 0.f;
+                const long long tb0 = (long long)t * KB;
+                const int c0 = tc_owner(tb0, T, P), c1 = tc_owner(tb0 + KB - 1, T, P);
+                // contributors in CTA order; each group's loads are issued together
+                constexpr int G = NACC == 1 ? 4 : NACC == 2 ? 2 : 1;
+                for (int cg = c0; cg <= c1; cg += G) {
+                    float u[G][NACC][16];
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const int cc = cg + g;
+                        const long long b0 = cc <= c1 ? tc_begin(cc, T, P) : 0;
+                        const bool use = cc <= c1 && tc_begin(cc + 1, T, P) != b0;   // skip empty ranges
                         const float *pp = a.part + (size_t)(cc * 2 + (b0 >= tb0 ? 0 : 1)) * ACC * 128;
 #pragma unroll
-                        for (int mm = 0; mm < NMAT; ++mm)
+                        for (int mm = 0; mm < NACC; ++mm)
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[mm][i] += __ldcg(pp + (mm * NB + c + i) * 128 + m);
+                            for (int i = 0; i < 16; ++i)
+                                u[g][mm][i] = use ? __ldcg(pp + (mm * NB + c + i) * 128 + m) : 0.f;
                     }
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int mm = 0; mm < NACC; ++mm)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[mm][i] += u[g][mm][i];
                 }
             };
             bool last = whole;
@@ -390,19 +440,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                 if (lane == 0) mbar_arrive(&acce[ab]);
                 named_sync(1, 128);
                 if (threadIdx.x == 0) {
-                    __threadfence();
                     const int add = kb1 - kb0;
-                    const unsigned old = atomicAdd(a.tile_cnt + t, (unsigned)add);
-                    s_last = (int)old + add == KB;
+                    s_last = (int)atom_add_acq_rel(a.tile_cnt + t, (uint32_t)add) + add == KB;
                 }
                 named_sync(1, 128);
                 last = s_last != 0;
-                if (last) __threadfence();
             }
             if (last) {
-                const int j = t * 128 + m;   // output row of the tile (DOWN: column of d)
                 int id = -1;
                 if constexpr (!DOWN) {
+                    const int j = t * 128 + m;
                     if (j < n) {
                         id = a.idx ? __ldcg(a.idx + j) : j;
                         if (id < 0 || id >= a.f) id = -1;
@@ -411,24 +458,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                 const float bias = (id >= 0 && a.bias) ? __ldg(a.bias + id) : 0.f;
                 bool act = false;
                 for (int c = 0; c < NB; c += 16) {
-                    float v[NMAT][16];
+                    float v[NACC][16];
                     chunk(c, v);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int b = c + i;
                         if constexpr (DOWN) {
                             if (b < a.B) {
-                                const size_t o = (size_t)b * a.d + j;
-                                a.out[o] = (a.xin ? __ldcg(a.xin + o) : 0.f) + v[0][i];
+#pragma unroll
+                                for (int mm = 0; mm < NACC; ++mm) {
+                                    const size_t o = (size_t)b * a.d + (size_t)t * 128 * W + mm * 128 + m;
+                                    a.out[o] = (a.xin ? __ldcg(a.xin + o) : 0.f) + v[mm][i];
+                                }
                             }
                         } else if constexpr (MODE == TC_LOGITS) {
                             act |= id >= 0 && b < a.B && (v[0][i] + bias > a.tau);
                         } else {
+                            const int j = t * 128 + m;
                             float hv = 0.f;
                             if (b < a.B && id >= 0) {
                                 if constexpr (MODE == TC_PRED_HIDDEN) hv = fmaxf(v[0][i], 0.f);
                                 else if constexpr (MODE == TC_RELU) hv = fmaxf(v[0][i] + bias, 0.f);
-                                else hv = fmaxf(v[0][i] + bias, 0.f) * v[1][i];
+                                else hv = fmaxf(v[0][i] + bias, 0.f) * v[NMAT - 1][i];
                             }
                             if (j < a.ldo) {
                                 uint16_t hi, lo;
@@ -451,13 +502,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                     const int wi = (t * 128 + 32 * warp) >> 5;
                     if (lane == 0 && wi < nwords) a.maskw[wi] = word;
                     named_sync(1, 128);
-                    if (threadIdx.x == 0) {
-                        __threadfence();
-                        s_last = atomicAdd(a.done_cnt, 1u) == (unsigned)tiles - 1;
-                    }
+                    if (threadIdx.x == 0) s_last = atom_add_acq_rel(a.done_cnt, 1u) == (unsigned)tiles - 1;
                     named_sync(1, 128);
                     if (s_last) {
-                        __threadfence();
                         tc_compact(a.maskw, nwords, a.idx_out, a.count_out, s_wsum);
                         if (threadIdx.x == 0) *a.done_cnt = 0u;
                     }
@@ -520,8 +567,8 @@ __global__ void __launch_bounds__(256) k_tc_split(const float *__restrict__ x, i
     }
 }
 
-template <int WT>
-cudaError_t launch_tc_wt(int mode, int nb, const TcArgs &a, int grid, size_t smem, cudaStream_t s, bool pdl)
+template <int WT, int MODE>
+cudaError_t launch_tc_mode(int nb, int w, const TcArgs &a, int grid, size_t smem, cudaStream_t s, bool pdl)
 {
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t e = ensure_smem(kern, smem);
@@ -535,22 +582,20 @@ cudaError_t launch_tc_wt(int mode, int nb, const TcArgs &a, int grid, size_t sme
         L.nsm = grid;
         return launch_ex(L, kern, a);
     };
-#define PI_TC_NB(MODE)                                   \
-    switch (nb) {                                        \
-    case 16: return go(k_tc<WT, MODE, 16>);              \
-    case 32: return go(k_tc<WT, MODE, 32>);              \
-    case 64: return go(k_tc<WT, MODE, 64>);              \
-    case 128: return go(k_tc<WT, MODE, 128>);            \
-    }                                                    \
-    break;
-    switch (mode) {
-    case TC_PRED_HIDDEN: PI_TC_NB(TC_PRED_HIDDEN)
-    case TC_LOGITS: PI_TC_NB(TC_LOGITS)
-    case TC_GATED: PI_TC_NB(TC_GATED)
-    case TC_RELU: PI_TC_NB(TC_RELU)
-    case TC_DOWN: PI_TC_NB(TC_DOWN)
+    auto by_w = [&](auto nbc) -> cudaError_t {
+        constexpr int NB = decltype(nbc)::value;
+        if (w == 1) return go(k_tc<WT, MODE, NB, 1>);
+        if (w == 2) return go(k_tc<WT, MODE, NB, 2>);
+        if constexpr (MODE == TC_DOWN && NB <= 64)
+            if (w == 4) return go(k_tc<WT, MODE, NB, 4>);
+        return cudaErrorInvalidValue;
+    };
+    switch (nb) {
+    case 16: return by_w(std::integral_constant<int, 16>());
+    case 32: return by_w(std::integral_constant<int, 32>());
+    case 64: return by_w(std::integral_constant<int, 64>());
+    case 128: return by_w(std::integral_constant<int, 128>());
     }
-#undef PI_TC_NB
     return cudaErrorInvalidValue;
 }
 

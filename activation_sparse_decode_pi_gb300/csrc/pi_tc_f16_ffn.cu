@@ -1,0 +1,7 @@
+// pi_tc_f16_ffn.cu -- tensor-core batch >= 16 kernels, f16 weights, ffn products (see pi_tc.cuh).
+#include "pi_tc.cuh"
+
+namespace pi {
+template cudaError_t launch_tc_mode<2, 2>(int, int, const TcArgs &, int, size_t, cudaStream_t, bool);
+template cudaError_t launch_tc_mode<2, 3>(int, int, const TcArgs &, int, size_t, cudaStream_t, bool);
+}  // namespace pi
