@@ -139,8 +139,8 @@ struct pi_ffn {
     // tensor-core path (batch >= tc_min_b)
     bool tc_ok = false;
     int tc_min_b = 16, tc_nbmax = 0, tc_rpad = 0, tc_fpad = 0;
-    int tc_stages[5][4][3] = {};       // [mode][log2(NB / 16)][log2(w)]
-    size_t tc_smem[5][4][3] = {};
+    int tc_stages[5][4][2] = {};       // [mode][log2(NB / 16)][log2(w)]
+    size_t tc_smem[5][4][2] = {};
     int tc_kw = 1, tc_ds = 1, tc_stage_cap = TC_MAX_STAGES;   // tuning (PI_FFN_TC_KW / _DS / _STAGES)
     uint16_t *tc_uhi = nullptr, *tc_ulo = nullptr, *tc_hphi = nullptr, *tc_hplo = nullptr, *tc_hhi = nullptr,
              *tc_hlo = nullptr;
@@ -316,14 +316,13 @@ void plan_tc(pi_ffn_t *h)
         const char *v = std::getenv(name);
         return v && std::atoi(v) > 0 ? std::atoi(v) : def;
     };
-    h->tc_kw = env_int("PI_FFN_TC_KW", 1) >= 2 ? 2 : 1;
-    h->tc_ds = std::min(4, env_int("PI_FFN_TC_DS", 1));
-    if (h->tc_ds == 3) h->tc_ds = 2;
+    h->tc_kw = env_int("PI_FFN_TC_KW", 2) >= 2 ? 2 : 1;
+    h->tc_ds = env_int("PI_FFN_TC_DS", 2) >= 2 ? 2 : 1;
     h->tc_stage_cap = std::min(TC_MAX_STAGES, env_int("PI_FFN_TC_STAGES", TC_MAX_STAGES));
     const size_t avail = (size_t)optin > 2048 ? (size_t)optin - 2048 : 0;   // alignment slack + static barriers
     for (int mode = 0; mode < 5; ++mode)
         for (int i = 0; i < 4; ++i)
-            for (int wi = 0; wi < 3; ++wi) {
+            for (int wi = 0; wi < 2; ++wi) {
                 const int nb = 16 << i, w = 1 << wi;
                 const size_t stage = mode == TC_DOWN ? (size_t)w * 16384 + 2 * (size_t)nb * 128
                                                      : (mode == TC_GATED ? 2 : 1) * (size_t)w * 16384 +
@@ -347,7 +346,7 @@ int tc_width(const pi_ffn_t *h, int mode, int nb, int K)
 {
     if (mode == TC_DOWN) {
         int w = h->tc_ds;
-        while (w > 1 && (h->desc.d % (128 * w) || 2 * w * nb > 512)) w /= 2;
+        while (w > 1 && h->desc.d % (128 * w)) w /= 2;
         return w;
     }
     return h->tc_kw == 2 && K % 128 == 0 ? 2 : 1;
@@ -371,7 +370,7 @@ cudaError_t tc_launch(const pi_ffn_t *h, int mode, int nb, const TcArgs &a0, cud
     TcArgs a = a0;
     const int i = tc_nbi(nb);
     int w = tc_width(h, mode, nb, a.K);
-    int wi = w == 1 ? 0 : w == 2 ? 1 : 2;
+    int wi = w == 1 ? 0 : 1;
     if (h->tc_stages[mode][i][wi] < 2) {   // that width does not fit shared memory: one block per step
         w = 1;
         wi = 0;

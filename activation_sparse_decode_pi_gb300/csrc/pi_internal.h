@@ -86,8 +86,8 @@ struct TcArgs {
     int stages;
 };
 
-// w: 64-wide K blocks per pipeline step (row modes: 1, 2), or 128-column slices per
-// W_down^T tile (TC_DOWN: 1, 2, 4 with 2 * w * nb <= 512).
+// w: 64-wide K blocks per pipeline step (row modes), or 128-column slices per W_down^T
+// tile (TC_DOWN); 1 or 2.
 template <int WT, int MODE>
 cudaError_t launch_tc_mode(int nb, int w, const TcArgs &a, int grid, size_t smem, cudaStream_t s, bool pdl);
 #define PI_TC_EXTERN(WT, MODE) \

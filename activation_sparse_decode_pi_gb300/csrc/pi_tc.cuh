@@ -23,9 +23,9 @@
 // the tile's k-block count adds them in CTA order, so the result does not depend on
 // timing (only on the grid size).
 //
-// Roles: warps 0-3 drain the accumulators (TMEM lane quarter = warp), warps 4-7 copy
+// Roles: warps 0-3 drain the accumulators (TMEM lane quarter = warp), warps 4-11 copy
 // the operands into a shared-memory ring with cp.async (16 bytes a thread, swizzled
-// into the 128-byte canonical layouts), warp 8 owns TMEM and one of its threads issues
+// into the 128-byte canonical layouts), warp 12 owns TMEM and one of its threads issues
 // the MMAs. Accumulators are double-buffered so the drain overlaps the next tile.
 // Every wait is bounded (200 ms): on expiry the kernel records PI_ERR_TIMEOUT, stops,
 // waits for its own copies and products, frees its TMEM and returns.
@@ -38,7 +38,9 @@
 
 namespace pi {
 
-constexpr int TC_THREADS = 288;
+constexpr int TC_PROD = 384;                       // producer threads (warps 4..11)
+constexpr int TC_MMA_WARP = 4 + TC_PROD / 32;      // warp 12: TMEM owner and MMA issuer
+constexpr int TC_THREADS = 32 * (TC_MMA_WARP + 1);
 
 __host__ __device__ constexpr uint32_t tc_tmem_cols(uint32_t need)
 {
@@ -58,20 +60,6 @@ __device__ __forceinline__ long long tc_begin(int c, long long T, int P) { retur
 __device__ __forceinline__ int tc_owner(long long it, long long T, int P)
 {
     return (int)(((it + 1) * P + T - 1) / T - 1);
-}
-
-__device__ __forceinline__ void cp_async_wait_n(int n)
-{
-    switch (n) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    case 3: cp_async_wait<3>(); break;
-    case 4: cp_async_wait<4>(); break;
-    case 5: cp_async_wait<5>(); break;
-    case 6: cp_async_wait<6>(); break;
-    default: cp_async_wait<7>(); break;
-    }
 }
 
 // Ascending compaction of the mask words by the 128 drain threads (named barrier 1).
@@ -120,22 +108,30 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v)
 }
 
 // W: 64-wide K blocks per pipeline step (row modes), or 128-column W_down^T slices per tile (TC_DOWN).
+//
+// Shared memory of one step: the weight blocks (16 KB each), then per K block the activation
+// tile as 2*NB rows, hi rows first, lo rows after: one MMA with N = 2*NB multiplies a weight
+// block by both halves, and the drain adds accumulator columns b and NB + b.
 template <int WT, int MODE, int NB, int W>
 __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
 {
     constexpr bool DOWN = MODE == TC_DOWN;
     constexpr int NMAT = MODE == TC_GATED ? 2 : 1;
-    constexpr int NACC = DOWN ? W : NMAT;                  // NB-wide accumulators per tile
+    constexpr int NACC = DOWN ? W : NMAT;                  // accumulators per tile
     constexpr int KW = DOWN ? 1 : W;                       // 64-wide K blocks per step
-    constexpr uint32_t BLK = 16384u;                       // one 128 x 64 (or 64 x 128) operand block
-    constexpr uint32_t XB = (uint32_t)NB * 128u;           // one NB x 64 activation block
+    constexpr uint32_t BLK = 16384u;                       // one 128 x 64 (or 64 x 128) weight block
+    constexpr uint32_t XB = (uint32_t)NB * 128u;           // one NB x 64 activation half
     constexpr uint32_t A_BYTES = (uint32_t)(DOWN ? W : NMAT * KW) * BLK;
     constexpr uint32_t STAGE = tc_stage_bytes(MODE, NB, W);
-    constexpr uint32_t ACC = (uint32_t)(NACC * NB);
-    constexpr uint32_t TCOLS = tc_tmem_cols(2 * ACC);
-    constexpr uint32_t IDESC = f16_idesc(WT == DT_BF16 ? 1 : 0, DOWN ? 1 : 0, 0, 128, NB);
+    constexpr uint32_t ACOLS = 2u * NB;                    // TMEM columns of one accumulator (hi | lo)
+    constexpr uint32_t ACC = (uint32_t)NACC * ACOLS;       // TMEM columns of one buffer
+    constexpr int NBUF = 2 * ACC <= 512 ? 2 : 1;           // accumulator buffers (drain overlaps the next tile)
+    constexpr uint32_t TCOLS = tc_tmem_cols(NBUF * ACC);
+    constexpr uint32_t PCOLS = (uint32_t)(NACC * NB);      // fp32 columns of one partial
+    constexpr uint32_t IDESC = f16_idesc(WT == DT_BF16 ? 1 : 0, DOWN ? 1 : 0, 0, 128, 2 * NB);
+    constexpr int CH = 1024 / TC_PROD + (1024 % TC_PROD ? 1 : 0);   // weight chunks per thread and block
     static_assert(NB % 16 == 0 && NB >= 16 && NB <= 128, "batch tile");
-    static_assert(2 * ACC <= 512, "accumulators exceed tensor memory");
+    static_assert(ACC <= 512, "accumulators exceed tensor memory");
     static_assert(A_BYTES + 2u * KW * XB == STAGE, "stage layout");
 
     extern __shared__ uint8_t dsm[];
@@ -148,11 +144,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
     const uint32_t sbase = (smem_u32(dsm) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = a.stages;
-    const int LAG = S - 1 < TC_MAX_STAGES - 1 ? S - 1 : TC_MAX_STAGES - 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 128);
+            mbar_init(&full[s], TC_PROD);
             mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -164,7 +159,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
         s_dabort = 0;
         fence_mbar_init();
     }
-    if (warp == 8) tmem_alloc(&tmem_base, TCOLS);
+    if (warp == TC_MMA_WARP) tmem_alloc(&tmem_base, TCOLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -193,40 +188,43 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
             a.out[e] = a.xin ? __ldcg(a.xin + e) : 0.f;
     }
 
-    if (warp >= 4 && warp < 8) {
+    if (warp >= 4 && warp < TC_MMA_WARP) {
         // ================================================================ producers
         const int p = threadIdx.x - 128;
         const uint16_t *const W0 = a.w0;
         uint32_t q = 0;
         bool bad = false;
-        auto step_done = [&]() {
-            cp_async_commit();
-            if (q >= (uint32_t)LAG) {
-                cp_async_wait_n(LAG);
-                fence_proxy_async_smem();
-                mbar_arrive(&full[(q - LAG) % S]);
+        // the step's slot is complete for the MMA when every producer's copies into it have
+        // landed: each thread's arrival is triggered by its own copies' completion
+        auto step_done = [&]() { cp_async_arrive_noinc(&full[q % S]); };
+        // activation tile of K block kb: NB hi rows then NB lo rows, 8 chunks of 16 bytes a row
+        auto load_x = [&](uint32_t xs, int kb) {
+            for (int c = p; c < 2 * NB * 8; c += TC_PROD) {
+                const int xr = c >> 3, xc = c & 7;
+                const uint16_t *src = (xr < NB ? a.xhi : a.xlo) + (size_t)(xr % NB) * a.ldx + kb * 64 + xc * 8;
+                cp_async16(xs + sw128_off(xr, xc), src, 16u);
             }
         };
         if constexpr (!DOWN) {
-            // 128 gathered rows x (KW x 64) columns per step; 8 threads per 128-byte row piece
-            const int prow = p >> 3, pch = p & 7;
-            const uint16_t *rp[NMAT][8];
+            // 128 gathered rows x (KW x 64) columns per step; chunk c = row * 8 + 16-byte piece
+            const uint16_t *rp[NMAT][CH];
             for (long long it = it0; it < it1 && !s_abort;) {
                 const int t = (int)(it / KB), kb0 = (int)(it - (long long)t * KB);
                 const int kb1 = (int)min((long long)KB, kb0 + (it1 - it));
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int j = t * 128 + prow + 16 * i;
+                for (int i = 0; i < CH; ++i) {
+                    const int c = p + TC_PROD * i;
+                    const int j = t * 128 + (c >> 3);
                     int id = -1;
-                    if (j < n) {
+                    if (c < 1024 && j < n) {
                         id = a.idx ? __ldcg(a.idx + j) : j;
                         if (id < 0 || id >= a.f) {
                             bad = true;
                             id = -1;
                         }
                     }
-                    rp[0][i] = id >= 0 ? W0 + (size_t)id * a.K : nullptr;
-                    if constexpr (NMAT == 2) rp[1][i] = id >= 0 ? a.w1 + (size_t)id * a.K : nullptr;
+                    rp[0][i] = id >= 0 ? W0 + (size_t)id * a.K + (c & 7) * 8 : nullptr;
+                    if constexpr (NMAT == 2) rp[1][i] = id >= 0 ? a.w1 + (size_t)id * a.K + (c & 7) * 8 : nullptr;
                 }
                 for (int kb = kb0; kb < kb1; ++kb, ++q) {
                     const int slot = (int)(q % (uint32_t)S);
@@ -238,43 +236,46 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                     const uint32_t st = sbase + (uint32_t)slot * STAGE;
 #pragma unroll
                     for (int w = 0; w < KW; ++w) {
-                        const int k0 = (kb * KW + w) * 64 + pch * 8;
+                        const int k0 = (kb * KW + w) * 64;
 #pragma unroll
                         for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const uint16_t *src = rp[m][i];
-                                cp_async16(st + (m * KW + w) * BLK + sw128_off(prow + 16 * i, pch), src ? src + k0 : W0,
-                                           src ? 16u : 0u);
+                            for (int i = 0; i < CH; ++i) {
+                                const int c = p + TC_PROD * i;
+                                if (c < 1024) {
+                                    const uint16_t *src = rp[m][i];
+                                    cp_async16(st + (m * KW + w) * BLK + sw128_off(c >> 3, c & 7), src ? src + k0 : W0,
+                                               src ? 16u : 0u);
+                                }
                             }
-                        const uint32_t xs = st + A_BYTES + w * XB;
-#pragma unroll
-                        for (int i = 0; i < NB / 16; ++i) {
-                            const int xb = prow + 16 * i;
-                            const size_t go = (size_t)xb * a.ldx + k0;
-                            cp_async16(xs + sw128_off(xb, pch), a.xhi + go, 16u);
-                            cp_async16(xs + KW * XB + sw128_off(xb, pch), a.xlo + go, 16u);
-                        }
+                        load_x(st + A_BYTES + 2 * w * XB, kb * KW + w);
                     }
                     step_done();
                 }
                 it += kb1 - kb0;
             }
         } else {
-            // W_down^T: 64 neuron rows x (W x 128) columns per step; 16 threads per 256-byte row piece
-            const int prow = p >> 4, pch = p & 15;
-            const int xrow = p >> 3, xch = p & 7;
-            int ids[8];   // the step's neuron ids; -2 marks the zero rows past the list's end
-            auto load_ids = [&](long long it) {
-                const int kb = (int)(it % KB);
+            // W_down^T: 64 neuron rows x (W x 128) columns per step; chunk c = row * 16 + 16-byte piece.
+            // Neuron ids of the next ID_AHEAD steps live in registers, so the list reads overlap the
+            // copies instead of stalling each step; -2 marks the zero rows past the list's end.
+            constexpr int ID_AHEAD = 4;
+            int ids[ID_AHEAD][CH];
+            auto load_ids = [&](long long it, int (&dst)[CH]) {
+                const int kb = it < it1 ? (int)(it % KB) : 0;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int j = kb * 64 + prow + 8 * i;
-                    ids[i] = j < n ? __ldcg(a.idx + j) : -2;
+                for (int i = 0; i < CH; ++i) {
+                    const int c = p + TC_PROD * i;
+                    const int j = kb * 64 + (c >> 4);
+                    dst[i] = (it < it1 && c < 1024 && j < n) ? __ldcg(a.idx + j) : -2;
                 }
             };
-            if (it0 < it1) load_ids(it0);
-            for (long long it = it0; it < it1 && !s_abort; ++it, ++q) {
+#pragma unroll
+            for (int u = 0; u < ID_AHEAD; ++u) load_ids(it0 + u, ids[u]);
+            for (long long its = it0; its < it1 && !s_abort; its += ID_AHEAD)
+#pragma unroll
+            for (int u = 0; u < ID_AHEAD; ++u) {
+                const long long it = its + u;
+                if (it >= it1 || s_abort) break;
                 const int t = (int)(it / KB), kb = (int)(it - (long long)t * KB);
                 const int slot = (int)(q % (uint32_t)S);
                 if (q >= (uint32_t)S && !mbar_wait(&empty[slot], ((q / S) - 1) & 1)) {
@@ -283,47 +284,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                     break;
                 }
                 const uint32_t st = sbase + (uint32_t)slot * STAGE;
-                const uint16_t *src[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    int id = ids[i];
+                for (int i = 0; i < CH; ++i) {
+                    const int c = p + TC_PROD * i;
+                    if (c >= 1024) continue;
+                    int id = ids[u][i];
                     if (id >= a.f || id < -2 || id == -1) {
                         bad = true;
                         id = -2;
                     }
-                    src[i] = id >= 0 ? W0 + (size_t)id * a.d + (size_t)t * 128 * W + pch * 8 : nullptr;
+                    const uint16_t *src = id >= 0 ? W0 + (size_t)id * a.d + (size_t)t * 128 * W + (c & 15) * 8 : nullptr;
+                    const uint32_t dst = st + (uint32_t)((c & 15) >> 3) * 8192u + sw128_off(c >> 4, c & 7);
+#pragma unroll
+                    for (int w = 0; w < W; ++w) cp_async16(dst + w * BLK, src ? src + w * 128 : W0, src ? 16u : 0u);
                 }
-#pragma unroll
-                for (int w = 0; w < W; ++w)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        cp_async16(st + w * BLK + (uint32_t)(pch >> 3) * 8192u + sw128_off(prow + 8 * i, pch & 7),
-                                   src[i] ? src[i] + w * 128 : W0, src[i] ? 16u : 0u);
-                const uint32_t xs = st + A_BYTES;
-#pragma unroll
-                for (int i = 0; i < NB / 16; ++i) {
-                    const int xb = xrow + 16 * i;
-                    const size_t go = (size_t)xb * a.ldx + kb * 64 + xch * 8;
-                    cp_async16(xs + sw128_off(xb, xch), a.xhi + go, 16u);
-                    cp_async16(xs + XB + sw128_off(xb, xch), a.xlo + go, 16u);
-                }
-                if (it + 1 < it1) load_ids(it + 1);   // consumed next step: the load overlaps
+                load_x(st + A_BYTES, kb);
+                load_ids(it + ID_AHEAD, ids[u]);   // consumed ID_AHEAD steps later
                 step_done();
+                ++q;
             }
         }
         cp_async_wait_all();
-        fence_proxy_async_smem();
-        for (uint32_t k = q > (uint32_t)LAG ? q - LAG : 0; k < q; ++k) mbar_arrive(&full[k % S]);
         if (bad) set_status(a.status, ST_DEVICE_CHECK);
-    } else if (warp == 8) {
+    } else if (warp == TC_MMA_WARP) {
         // ================================================================ MMA issuer
         if (lane == 0) {
             uint32_t q = 0, si = 0;
             for (long long it = it0; it < it1 && !s_abort; ++si) {
                 const int t = (int)(it / KB), kb0 = (int)(it - (long long)t * KB);
                 const int kb1 = (int)min((long long)KB, kb0 + (it1 - it));
-                const uint32_t ab = si & 1;
-                if (si >= 2 && !mbar_wait(&acce[ab], ((si >> 1) - 1) & 1)) {
+                const uint32_t ab = si % NBUF;
+                if (si >= (uint32_t)NBUF && !mbar_wait(&acce[ab], ((si / NBUF) - 1) & 1)) {
                     set_status(a.status, ST_TIMEOUT);
                     s_abort = 1;
                     break;
@@ -337,25 +328,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                         s_abort = 1;
                         break;
                     }
+                    fence_proxy_async_smem();   // the producers' copies, seen through the barrier, to the tensor core
                     tc_fence_after();
                     const uint32_t st = sbase + (uint32_t)slot * STAGE;
+                    const uint64_t a0 = sw128_desc(st, DOWN ? 8192u : 16u, 1024u);
+                    const uint64_t x0 = sw128_desc(st + A_BYTES, 16u, 1024u);
 #pragma unroll
-                    for (int w = 0; w < KW; ++w) {
-                        const uint32_t xh = st + A_BYTES + w * XB, xl = xh + KW * XB;
+                    for (int w = 0; w < KW; ++w)
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const uint64_t bh = sw128_desc(xh + j * 32, 16, 1024);
-                            const uint64_t bl = sw128_desc(xl + j * 32, 16, 1024);
+                            // descriptor start addresses advance in 16-byte units
+                            const uint64_t bd = x0 + ((2 * w * XB + j * 32) >> 4);
                             const bool acc = kb > kb0 || w > 0 || j > 0;
 #pragma unroll
                             for (int m = 0; m < NACC; ++m) {
-                                const uint64_t ad = DOWN ? sw128_desc(st + m * BLK + j * 2048, 8192, 1024)
-                                                         : sw128_desc(st + (m * KW + w) * BLK + j * 32, 16, 1024);
-                                umma_f16(d0 + m * NB, ad, bh, IDESC, acc);
-                                umma_f16(d0 + m * NB, ad, bl, IDESC, true);
+                                const uint64_t ad = DOWN ? a0 + ((m * BLK + j * 2048) >> 4)
+                                                         : a0 + (((m * KW + w) * BLK + j * 32) >> 4);
+                                umma_f16(d0 + m * ACOLS, ad, bd, IDESC, acc);
                             }
                         }
-                    }
                     umma_commit(&empty[slot]);
                 }
                 if (s_abort) break;
@@ -374,9 +365,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
             const int t = (int)(it / KB), kb0 = (int)(it - (long long)t * KB);
             const int kb1 = (int)min((long long)KB, kb0 + (it1 - it));
             it += kb1 - kb0;
-            const uint32_t ab = si & 1;
+            const uint32_t ab = si % NBUF;
             // all four drain warps take the same decision, so none is left at a named barrier
-            if (!mbar_wait(&accf[ab], (si >> 1) & 1)) s_dabort = 1;
+            if (!mbar_wait(&accf[ab], (si / NBUF) & 1)) s_dabort = 1;
             named_sync(1, 128);
             if (s_dabort) {
                 if (threadIdx.x == 0) set_status(a.status, ST_TIMEOUT);
@@ -385,22 +376,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
             }
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(32 * warp) << 16) + ab * ACC;
+            // 16 columns of accumulator mm: hi-part products plus lo-part products
+            auto acc16 = [&](int mm, int c, float (&v)[16]) {
+                float lo[16];
+                tmem_ld16(tb + mm * ACOLS + c, v);
+                tmem_ld16(tb + mm * ACOLS + NB + c, lo);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] += lo[i];
+            };
             const bool whole = kb0 == 0 && kb1 == KB;
             if (!whole) {
                 const int slot = it0 >= (long long)t * KB ? 0 : 1;
-                float *mypart = a.part + (size_t)(cta * 2 + slot) * ACC * 128;
-                for (uint32_t c = 0; c < ACC; c += 16) {
-                    float v[16];
-                    tmem_ld16(tb + c, v);
+                float *mypart = a.part + (size_t)(cta * 2 + slot) * PCOLS * 128;
+#pragma unroll 1
+                for (int mm = 0; mm < NACC; ++mm)
+#pragma unroll 1
+                    for (int c = 0; c < NB; c += 16) {
+                        float v[16];
+                        acc16(mm, c, v);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) mypart[(c + i) * 128 + m] = v[i];
-                }
+                        for (int i = 0; i < 16; ++i) mypart[(mm * NB + c + i) * 128 + m] = v[i];
+                    }
             }
             // the tile's final values, 16 batch columns at a time, from TMEM or from the partials
             auto chunk = [&](int c, float (&v)[NACC][16]) {
                 if (whole) {
 #pragma unroll
-                    for (int mm = 0; mm < NACC; ++mm) tmem_ld16(tb + mm * NB + c, v[mm]);
+                    for (int mm = 0; mm < NACC; ++mm) acc16(mm, c, v[mm]);
                     return;
                 }
 #pragma unroll
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                 const long long tb0 = (long long)t * KB;
                 const int c0 = tc_owner(tb0, T, P), c1 = tc_owner(tb0 + KB - 1, T, P);
                 // contributors in CTA order; each group's loads are issued together
-                constexpr int G = NACC == 1 ? 4 : NACC == 2 ? 2 : 1;
+                constexpr int G = NACC == 1 ? 2 : 1;
                 for (int cg = c0; cg <= c1; cg += G) {
                     float u[G][NACC][16];
 #pragma unroll
@@ -418,7 +420,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                         const int cc = cg + g;
                         const long long b0 = cc <= c1 ? tc_begin(cc, T, P) : 0;
                         const bool use = cc <= c1 && tc_begin(cc + 1, T, P) != b0;   // skip empty ranges
-                        const float *pp = a.part + (size_t)(cc * 2 + (b0 >= tb0 ? 0 : 1)) * ACC * 128;
+                        const float *pp = a.part + (size_t)(cc * 2 + (b0 >= tb0 ? 0 : 1)) * PCOLS * 128;
 #pragma unroll
                         for (int mm = 0; mm < NACC; ++mm)
 #pragma unroll
@@ -457,6 +459,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                 }
                 const float bias = (id >= 0 && a.bias) ? __ldg(a.bias + id) : 0.f;
                 bool act = false;
+#pragma unroll 1
                 for (int c = 0; c < NB; c += 16) {
                     float v[NACC][16];
                     chunk(c, v);
@@ -516,7 +519,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
     // ---- teardown: all copies and products of this CTA are complete
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == TC_MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, TCOLS);
     }
@@ -586,8 +589,6 @@ cudaError_t launch_tc_mode(int nb, int w, const TcArgs &a, int grid, size_t smem
         constexpr int NB = decltype(nbc)::value;
         if (w == 1) return go(k_tc<WT, MODE, NB, 1>);
         if (w == 2) return go(k_tc<WT, MODE, NB, 2>);
-        if constexpr (MODE == TC_DOWN && NB <= 64)
-            if (w == 4) return go(k_tc<WT, MODE, NB, 4>);
         return cudaErrorInvalidValue;
     };
     switch (nb) {
