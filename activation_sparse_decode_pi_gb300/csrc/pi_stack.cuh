@@ -203,9 +203,22 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             const uint4 *row[5];
             const __half *srow[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
             RowChunks<PT, 5, 4> rc;
+            // hp is requested first, so its reads (L2 hits) do not queue behind the P2 rows
+            const int r4 = r / 4;
+            float4 hv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = tid + u * STACK_NT;
+                hv[u] = t < r4 ? __ldcg(reinterpret_cast<const float4 *>(a.hp) + t) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             owned_rows<5>(row, Lw.p2, warp, SNW, K, c, P, nchr);
             rows_issue(rc, row, srow, lane, nchr);                  // before hp is staged
-            stage_planar<PT, 1>(hp4, a.hp, r, 1, nullptr);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                constexpr int QH = VP / 4;
+                const int t = tid + u * STACK_NT;
+                if (t < r4) hp4[(t % QH) * nchr + t / QH] = hv[u];   // planar layout of the row dot products
+            }
             __syncthreads();
             for (int kbase = warp; kbase < K; kbase += SNW * 5) {
                 if (kbase != warp) {
@@ -273,9 +286,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 }
                 if (bias_bulk) bulk_g2s(sl + bias_off, Lw.bg + (i & ~3), 16, mb);
             };
-            if (tid == 0) {
+            // one issuing thread per neuron (lane 0 of warp m % SNW): the copies leave in parallel
+            if (lane == 0 && warp < nn) {
                 fence_proxy_async_smem();
-                for (int m = 0; m < nn && m < S; ++m) issue(seq + m, sneur[m]);
+                for (int m = warp; m < nn && m < S; m += SNW) issue(seq + m, sneur[m]);
             }
             // this thread's columns of u, scaled (loaded while the first rows are in flight)
             float ur[CPT][VW];
@@ -368,10 +382,12 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     return;
                 }
                 // the previous batch's slots are free: refill them
-                if (tid == 0 && m0 > 0) {
-                    fence_proxy_async_smem();
-                    for (int k = m0 - nb; k < m0; ++k)
-                        if (k + S < nn) issue(seq + k + S, sneur[k + S]);
+                if (m0 > 0 && lane == 0 && warp < nb) {
+                    const int k = m0 - nb + warp;
+                    if (k + S < nn) {
+                        fence_proxy_async_smem();
+                        issue(seq + k + S, sneur[k + S]);
+                    }
                 }
 #pragma unroll
                 for (int k = 0; k < NB; ++k) {
