@@ -130,6 +130,7 @@ struct pi_ffn {
     size_t prof_n = 0;
     // persistent decode-step kernel (batch 1)
     bool stack_ok = false;
+    int n_hot = 0;                     // neurons [0, n_hot) expected to fire on most tokens
     StackLayer *stack_layers = nullptr;
     uint32_t *stack_mask = nullptr;
     float *stack_sumsq = nullptr;
@@ -630,6 +631,8 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.off_flags = h->off_flags;
     a.off_mbar = h->off_mbar;
     a.ring_bytes = h->stack_ring;
+    a.hot_k = h->n_hot > 0 ? std::min((h->n_hot + h->nsm - 1) / h->nsm, h->stack_slots - 2) : 0;
+    if (a.hot_k < 0) a.hot_k = 0;
     a.bias_bulk = D.f % 4 == 0 ? 1 : 0;
     for (const pi_layer_weights_t &w : h->layers)
         if (!w.b_gate) a.bias_bulk = 0;
@@ -874,6 +877,13 @@ pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_ou
         h->g_idx = idx_out;
     }
     return cuda_status(cudaGraphLaunch(h->gexec, st));
+}
+
+pi_status_t pi_ffn_set_hot_neurons(pi_ffn_t *h, int32_t n_hot)
+{
+    if (!h || n_hot < 0 || n_hot > h->desc.f) return PI_ERR_INVALID_ARG;
+    h->n_hot = n_hot;
+    return PI_OK;
 }
 
 pi_status_t pi_profile_begin(pi_ffn_t *h)

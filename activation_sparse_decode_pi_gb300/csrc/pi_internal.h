@@ -52,6 +52,7 @@ struct StackArgs {
     int off_ua, off_hp, off_scr, off_flags, off_mbar, off_ring;   // dynamic shared-memory layout
     int ring_bytes;               // ring region: the neuron slots
     int bias_bulk;                // gate biases ride in the row copies (every layer has one and f % 4 == 0)
+    int hot_k;                    // ring slots per CTA held by hot owned neurons (loaded a layer ahead), <= slots - 2
 };
 
 template <int WT>

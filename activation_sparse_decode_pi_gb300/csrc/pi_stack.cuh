@@ -25,6 +25,11 @@
 // The predictor weights do not depend on the input: each CTA prefetches its predictor
 // slice of the next layer into L2 while the current layer runs, and requests its P1
 // rows before it stages u.
+// Hot neurons (the first hot_k owned ones in hot-first order, typically active on most
+// tokens) have ring slots of their own: their rows are requested one layer ahead, during the
+// previous layer's reduction phase, before the predictor has said whether they fire. A hot
+// neuron the predictor rejects costs its bytes and nothing else: the neurons are reduced in
+// the same list order either way, so the output bits do not depend on hot_k.
 // The result is deterministic: every sum runs in a fixed order for a given grid size.
 #pragma once
 
@@ -70,6 +75,32 @@ __device__ __forceinline__ void owned_rows(const uint4 *(&row)[RW], const void *
     }
 }
 
+// Bulk-copy neuron i's rows of layer Lw (gate(, up), W_down; int4 scales; the 16-byte chunk
+// holding its gate bias) into ring slot `slot`; completion is counted on the slot's mbarrier.
+// Everything is derived from the launch arguments, so callers keep no state for it.
+template <int WT, int KIND>
+__device__ __forceinline__ void stage_neuron(const StackArgs &a, const StackLayer &Lw, unsigned char *ring,
+                                             uint64_t *mbar, int slot, int i)
+{
+    constexpr int ROWS = KIND == KIND_GATED ? 3 : 2;
+    const int rowb = WT == DT_F32 ? a.d * 4 : (WT == DT_INT4 ? a.d / 2 : a.d * 2);
+    const int sclb = WT == DT_INT4 ? (a.d / 128) * 2 : 0;
+    const int bias_off = ROWS * (rowb + sclb);
+    unsigned char *sl = ring + (size_t)slot * a.slot_bytes;
+    uint64_t *mb = &mbar[slot];
+    mbar_arrive_expect_tx(mb, (uint32_t)(bias_off + (a.bias_bulk ? 16 : 0)));
+    bulk_g2s(sl, (const char *)Lw.wg + (size_t)i * rowb, rowb, mb);
+    if (KIND == KIND_GATED) bulk_g2s(sl + rowb, (const char *)Lw.wu + (size_t)i * rowb, rowb, mb);
+    bulk_g2s(sl + (ROWS - 1) * rowb, (const char *)Lw.wd + (size_t)i * rowb, rowb, mb);
+    if (WT == DT_INT4) {
+        unsigned char *ss = sl + ROWS * rowb;
+        bulk_g2s(ss, (const char *)Lw.sg + (size_t)i * sclb, sclb, mb);
+        if (KIND == KIND_GATED) bulk_g2s(ss + sclb, (const char *)Lw.su + (size_t)i * sclb, sclb, mb);
+        bulk_g2s(ss + (ROWS - 1) * sclb, (const char *)Lw.sd + (size_t)i * sclb, sclb, mb);
+    }
+    if (a.bias_bulk) bulk_g2s(sl + bias_off, Lw.bg + (i & ~3), 16, mb);
+}
+
 template <int WT, int PT, int KIND, int CPT>
 __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 {
@@ -104,7 +135,11 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     const int K = c < f ? (f - 1 - c) / P + 1 : 0;          // owned neurons: i = c + P * k, k < K
     const int bias_off = ROWS * (rowb + sclb);               // 16-byte chunk holding the gate bias
     const bool bias_bulk = a.bias_bulk != 0;                 // the chunk stays inside b_gate only if f % 4 == 0
-    uint32_t seq = 0;   // neurons staged by this CTA so far: slot seq % S, phase (seq / S) & 1
+    // Ring slots [0, HK) hold this CTA's hot owned neurons k < HK (loaded every layer before its
+    // predictor runs: the copy for layer l is the slot's l-th, parity l & 1). Slots [HK, S) take
+    // the other active neurons in list order: the cold neuron staged n-th in this launch goes to
+    // slot HK + n % SC with parity (n / SC) & 1.
+    uint32_t cseq = 0;
     unsigned kb = 0;    // grid barriers passed in this launch
     auto sync_grid = [&]() -> bool {
         ++kb;
@@ -116,9 +151,25 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     const int pa_per = (nchp + SNW - 1) / SNW, pa_cb = warp * pa_per, pa_ce = min(nchp, pa_cb + pa_per);
     RowChunks<PT, 8, 1> pa;
     // the rest of this CTA's predictor slice, into L2
+    // (one prefetch per thread: thread k < K takes owned P2 row k, the last thread the P1 rows)
     auto prefetch_predictor = [&](const StackLayer &L) {
-        prefetch_l2_range((const char *)L.p1 + (size_t)k0 * d * pb, (size_t)(k1 - k0) * d * pb);
-        for (int k = 0; k < K; ++k) prefetch_l2((const char *)L.p2 + (size_t)(c + (size_t)P * k) * r * pb, r * pb);
+        if (tid < K) prefetch_l2((const char *)L.p2 + (size_t)(c + (size_t)P * tid) * r * pb, r * pb);
+        if (tid == STACK_NT - 1) prefetch_l2_range((const char *)L.p1 + (size_t)k0 * d * pb, (size_t)(k1 - k0) * d * pb);
+    };
+
+    // the hot owned neurons of layer Lw into their slots, one issuing thread per neuron; the
+    // slots' previous copies (parity prev, or none when prev < 0) have landed and been read
+    auto issue_hot = [&](const StackLayer &Lw, int prev) {
+        const int w = threadIdx.x >> 5, cb = blockIdx.x, np = gridDim.x;
+        const int hk = min(a.hot_k, cb < a.f ? (a.f - 1 - cb) / np + 1 : 0);
+        if ((threadIdx.x & 31) != 0 || w >= hk) return;
+        unsigned char *rg = smem + a.off_ring;
+        uint64_t *mbs = reinterpret_cast<uint64_t *>(smem + a.off_mbar);
+        for (int k = w; k < hk; k += SNW) {
+            if (prev >= 0 && !mbar_wait(&mbs[k], (uint32_t)prev & 1u)) set_status(a.status, ST_TIMEOUT);
+            fence_proxy_async_smem();
+            stage_neuron<WT, KIND>(a, Lw, rg, mbs, k, cb + np * k);
+        }
     };
 
     // ---------------------------------------------------------------- phase 0
@@ -126,8 +177,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
         for (int s = 0; s < S; ++s) mbar_init(&mbar[s], 1);
         fence_mbar_init();
         s_base = barrier_base(a.bar, (unsigned long long)(3 * a.L) * a.nblocks);
-        prefetch_predictor(a.layers[0]);
     }
+    prefetch_predictor(a.layers[0]);
+    __syncthreads();
+    issue_hot(a.layers[0], -1);
     if (a.idx_out)
         for (int i = c * STACK_NT + tid; i < a.L * W; i += P * STACK_NT) a.maskw[i] = 0u;
     if (a.counts && c == 0)
@@ -166,7 +219,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 ua4[q * nchp + ci] = v;
             }
             __syncthreads();
-            if (tid == 0 && l + 1 < a.L) prefetch_predictor(a.layers[l + 1]);
+            if (l + 1 < a.L) prefetch_predictor(a.layers[l + 1]);
             const uint4 *row[8];
             const __half *srow[8];
 #pragma unroll
@@ -270,26 +323,26 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             if (tid == 0 && a.counts && nn) atomicAdd(a.counts + l, nn);
             __syncthreads();
 
-            auto issue = [&](uint32_t sq, int i) {
-                const int slot = (int)(sq % (uint32_t)S);
-                unsigned char *sl = ring + (size_t)slot * a.slot_bytes;
-                uint64_t *mb = &mbar[slot];
-                mbar_arrive_expect_tx(mb, (uint32_t)(bias_off + (bias_bulk ? 16 : 0)));
-                bulk_g2s(sl, (const char *)Lw.wg + (size_t)i * rowb, rowb, mb);
-                if (KIND == KIND_GATED) bulk_g2s(sl + rowb, (const char *)Lw.wu + (size_t)i * rowb, rowb, mb);
-                bulk_g2s(sl + (ROWS - 1) * rowb, (const char *)Lw.wd + (size_t)i * rowb, rowb, mb);
-                if (WT == DT_INT4) {
-                    unsigned char *ss = sl + ROWS * rowb;
-                    bulk_g2s(ss, (const char *)Lw.sg + (size_t)i * sclb, sclb, mb);
-                    if (KIND == KIND_GATED) bulk_g2s(ss + sclb, (const char *)Lw.su + (size_t)i * sclb, sclb, mb);
-                    bulk_g2s(ss + (ROWS - 1) * sclb, (const char *)Lw.sd + (size_t)i * sclb, sclb, mb);
+            // list entries [0, nh) are hot (already in their slots), [nh, nn) cold
+            const int HK = a.hot_k, SC = S - HK, hk = min(HK, K);
+            int nh = 0;
+            while (nh < nn && (sneur[nh] - c) / P < hk) ++nh;
+            auto slot_of = [&](int m, uint32_t &par) -> int {
+                if (m < nh) {
+                    par = (uint32_t)l & 1u;
+                    return (sneur[m] - c) / P;
                 }
-                if (bias_bulk) bulk_g2s(sl + bias_off, Lw.bg + (i & ~3), 16, mb);
+                const uint32_t sq = cseq + (uint32_t)(m - nh);
+                par = (sq / (uint32_t)SC) & 1u;
+                return HK + (int)(sq % (uint32_t)SC);
             };
-            // one issuing thread per neuron (lane 0 of warp m % SNW): the copies leave in parallel
-            if (lane == 0 && warp < nn) {
+            // the first cold neurons, one issuing thread per neuron (lane 0 of warp (m - nh) % SNW)
+            if (lane == 0 && nh + warp < nn) {
                 fence_proxy_async_smem();
-                for (int m = warp; m < nn && m < S; m += SNW) issue(seq + m, sneur[m]);
+                for (int m = nh + warp; m < nn && m < nh + SC; m += SNW) {
+                    uint32_t par;
+                    stage_neuron<WT, KIND>(a, Lw, ring, mbar, slot_of(m, par), sneur[m]);
+                }
             }
             // this thread's columns of u, scaled (loaded while the first rows are in flight)
             float ur[CPT][VW];
@@ -313,12 +366,15 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 #pragma unroll
                 for (int e = 0; e < VW; ++e) yr[cc][e] = 0.f;
 
-            // neurons are reduced nb at a time: one CTA-wide synchronisation per batch. A batch
-            // waits only on copies issued at least one batch earlier, which needs 2 * nb <= S.
+            // neurons are reduced a batch at a time, in list order (hot ones first): one CTA-wide
+            // synchronisation per batch. Hot batches take up to NB resident neurons; a cold batch
+            // waits only on copies issued at least one batch earlier, which needs 2 * nbc <= SC.
             constexpr int NB = 4;
-            const int nb = max(1, min(NB, S / 2));
-            for (int m0 = 0, bi = 0; m0 < nn; m0 += nb, ++bi) {
-                const int mb = min(nb, nn - m0);
+            const int nbc = max(1, min(NB, SC / 2));
+            int bi = 0;
+            for (int m0 = 0; m0 < nn; ++bi) {
+                const bool cold = m0 >= nh;
+                const int mb = cold ? min(nbc, nn - m0) : min(NB, nh - m0);
                 bool got = true;
                 float pg[NB], pu[NB];
 #pragma unroll
@@ -326,9 +382,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     pg[k] = 0.f;
                     pu[k] = 0.f;
                     if (k >= mb) continue;
-                    const uint32_t sq = seq + m0 + k;
-                    const unsigned char *sl = ring + (size_t)(sq % (uint32_t)S) * a.slot_bytes;
-                    got = got && mbar_wait(&mbar[sq % (uint32_t)S], (sq / (uint32_t)S) & 1u);
+                    uint32_t par;
+                    const int slot = slot_of(m0 + k, par);
+                    const unsigned char *sl = ring + (size_t)slot * a.slot_bytes;
+                    got = got && mbar_wait(&mbar[slot], par);
                     if (!got) continue;
 #pragma unroll
                     for (int cc = 0; cc < CPT; ++cc) {
@@ -376,24 +433,29 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     // give up: wait (bounded) for this CTA's copies still in flight, then leave
                     if (tid == 0) {
                         set_status(a.status, ST_TIMEOUT);
-                        for (int k = m0; k < nn && k < m0 + S; ++k)
-                            mbar_wait(&mbar[(seq + k) % (uint32_t)S], ((seq + k) / (uint32_t)S) & 1u);
+                        for (int k = 0; k < hk; ++k) mbar_wait(&mbar[k], (uint32_t)l & 1u);
+                        for (int k = max(m0, nh); k < nn && k < max(m0, nh) + SC; ++k) {
+                            uint32_t par;
+                            const int slot = slot_of(k, par);
+                            mbar_wait(&mbar[slot], par);
+                        }
                     }
                     return;
                 }
-                // the previous batch's slots are free: refill them
-                if (m0 > 0 && lane == 0 && warp < nb) {
-                    const int k = m0 - nb + warp;
-                    if (k + S < nn) {
+                // the previous cold batch's slots are free: refill them
+                if (cold && m0 - nbc >= nh && lane == 0 && warp < nbc) {
+                    const int k = m0 - nbc + warp;
+                    if (k + SC < nn) {
                         fence_proxy_async_smem();
-                        issue(seq + k + S, sneur[k + S]);
+                        uint32_t par;
+                        stage_neuron<WT, KIND>(a, Lw, ring, mbar, slot_of(k + SC, par), sneur[k + SC]);
                     }
                 }
 #pragma unroll
                 for (int k = 0; k < NB; ++k) {
                     if (k >= mb) break;
-                    const uint32_t sq = seq + m0 + k;
-                    const unsigned char *sl = ring + (size_t)(sq % (uint32_t)S) * a.slot_bytes;
+                    uint32_t par;
+                    const unsigned char *sl = ring + (size_t)slot_of(m0 + k, par) * a.slot_bytes;
                     float g = 0.f, up = 0.f;
                     for (int w = 0; w < SNW; ++w) {   // fixed order
                         g += red[bi & 1][w][2 * k];
@@ -422,8 +484,9 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                         }
                     }
                 }
+                m0 += mb;
             }
-            seq += (uint32_t)nn;
+            cseq += (uint32_t)(nn - nh);
             float *pq = a.part + (size_t)c * d;
 #pragma unroll
             for (int cc = 0; cc < CPT; ++cc) {
@@ -433,6 +496,12 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 for (int e4 = 0; e4 < VW / 4; ++e4)
                     reinterpret_cast<float4 *>(pq + (size_t)ci * VW)[e4] =
                         make_float4(yr[cc][4 * e4], yr[cc][4 * e4 + 1], yr[cc][4 * e4 + 2], yr[cc][4 * e4 + 3]);
+            }
+            // every thread is done with the ring: the next layer's hot rows can be requested now,
+            // a whole layer before their predictor runs
+            if (l + 1 < a.L && a.hot_k > 0) {
+                __syncthreads();
+                issue_hot(a.layers[l + 1], l);
             }
         }
         if (!sync_grid()) return;
@@ -506,6 +575,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             }
         }
     }
+    // the last layer's hot copies of neurons that were not active have landed before the CTA leaves
+    if (lane == 0)
+        for (int k = warp; k < min(a.hot_k, K); k += SNW)
+            if (!mbar_wait(&mbar[k], (uint32_t)(a.L - 1) & 1u)) set_status(a.status, ST_TIMEOUT);
 }
 
 template <int WT>

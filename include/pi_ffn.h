@@ -244,6 +244,19 @@ pi_status_t pi_selftest_grid_barrier(uint32_t *work, int32_t extra, void *stream
 pi_status_t pi_selftest_umma(const void *a, const void *b, float *d, int32_t mode, int32_t n, int32_t k,
                              int32_t dtype, uint32_t *status, void *stream);
 
+/*
+ * Hot neurons of the batch-1 decode step. The offline profile ("PowerInfer" paper
+ * walk-through, offline profiling code block; summary page, Methodology: a small set of
+ * hot neurons fires on most inputs) orders neurons hot-first; n_hot says that neurons
+ * [0, n_hot) fire on most tokens. The persistent batch-1 kernel of pi_decode_stack then
+ * requests those neurons' rows one layer ahead, before their predictor has run, into ring
+ * slots of their own (at most ring slots - 2 per SM). A hot neuron that the predictor
+ * rejects costs its bytes but does not change the result: the output is bit-identical for
+ * every n_hot. 0 (the default) turns this off. Other paths ignore it.
+ * Returns PI_ERR_INVALID_ARG unless 0 <= n_hot <= f. Takes effect from the next call.
+ */
+pi_status_t pi_ffn_set_hot_neurons(pi_ffn_t *h, int32_t n_hot);
+
 /* Wait for all work on the device, return the first kernel-recorded error and clear it. */
 pi_status_t pi_get_status(pi_ffn_t *h);
 

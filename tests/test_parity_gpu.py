@@ -333,3 +333,33 @@ def test_grid_barrier_gives_up_cleanly(P):
     assert torch.isfinite(xo).all()
     assert ffn.status() == 0
     ffn.close()
+
+
+@pytest.mark.parametrize("wi", range(5))
+def test_decode_stack_hot_neurons_bit_identical(P, wi):
+    """Requesting the hot neurons' rows a layer ahead changes nothing in the output bits."""
+    w = _wl(wi, STACK_SHAPE, n_layers=3)
+    layers = build_layers(w, range(w.n_layers))
+    X = make_inputs(w, 3, 1, seed=11, device="cpu").numpy()
+    ffn = _handle(P, w, [g for g, _ in layers], stack_kernel=True)
+    ref = []
+    for t in range(X.shape[0]):
+        counts = torch.zeros(w.n_layers, dtype=torch.int32, device="cuda")
+        idx_out = torch.zeros((w.n_layers, w.f), dtype=torch.int32, device="cuda")
+        xo = ffn.decode_stack(to_dev(X[t]), counts=counts, idx_out=idx_out)
+        ref.append((xo.clone(), counts.clone(), idx_out.clone()))
+    for n_hot in (1, 250, 700, w.f):
+        ffn.set_hot_neurons(n_hot)
+        for t in range(X.shape[0]):
+            counts = torch.zeros(w.n_layers, dtype=torch.int32, device="cuda")
+            idx_out = torch.zeros((w.n_layers, w.f), dtype=torch.int32, device="cuda")
+            P.pi_profile_begin(ffn.h)
+            xo = ffn.decode_stack(to_dev(X[t]), counts=counts, idx_out=idx_out)
+            prof = P.pi_profile_end(ffn.h)
+            assert prof["decode_stack"][1] == 1, prof
+            assert torch.equal(xo, ref[t][0]), (n_hot, t)
+            assert torch.equal(counts, ref[t][1]) and torch.equal(idx_out, ref[t][2]), (n_hot, t)
+    with pytest.raises(P.PiError):
+        ffn.set_hot_neurons(w.f + 1)
+    assert ffn.status() == 0
+    ffn.close()
