@@ -81,44 +81,6 @@ k_pred_hidden(const uint4 *__restrict__ P1, int d, int r, const float *__restric
     }
 }
 
-// ---------------------------------------------------------------- compaction -----------------
-// Ascending list of the set bits of nwords mask words (one CTA of NT threads).
-__device__ void compact_mask(const uint32_t *__restrict__ maskw, int nwords, int32_t *__restrict__ idx,
-                             int32_t *__restrict__ count)
-{
-    __shared__ int wsum[NW];
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int per = (nwords + NT - 1) / NT;
-    const int w0 = t * per, w1 = min(nwords, w0 + per);
-    int mine = 0;
-    for (int i = w0; i < w1; ++i) mine += __popc(__ldcg(maskw + i));
-    // block-wide exclusive scan of `mine`
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    int before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-        before += w < warp ? wsum[w] : 0;
-        total += wsum[w];
-    }
-    int off = before + incl - mine;
-    for (int i = w0; i < w1; ++i) {
-        uint32_t m = __ldcg(maskw + i);
-        while (m) {
-            const int bit = __ffs(m) - 1;
-            idx[off++] = i * 32 + bit;
-            m &= m - 1;
-        }
-    }
-    if (t == 0) *count = total;
-}
-
 // ---------------------------------------------------------------- K2 -------------------------
 // CTA: 8 warps, 32 consecutive neurons (one mask word); warp w takes neurons w, w+8, w+16, w+24.
 template <int PT, int BT>
@@ -190,7 +152,8 @@ k_pred_logits(const uint4 *__restrict__ P2, int r, int f, const float *__restric
     __syncthreads();
     if (!last) return;
     __threadfence();
-    compact_mask(maskw, gridDim.x, idx, count);
+    __shared__ int wsum[NW];
+    compact_words<NW>(maskw, gridDim.x, idx, count, wsum, [] { __syncthreads(); });
     if (threadIdx.x == 0) *ticket = 0u;
 }
 

@@ -62,42 +62,6 @@ __device__ __forceinline__ int tc_owner(long long it, long long T, int P)
     return (int)(((it + 1) * P + T - 1) / T - 1);
 }
 
-// Ascending compaction of the mask words by the 128 drain threads (named barrier 1).
-__device__ __forceinline__ void tc_compact(const uint32_t *__restrict__ maskw, int nwords, int32_t *__restrict__ idx,
-                                           int32_t *__restrict__ count, int *wsum)
-{
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int per = (nwords + 127) / 128;
-    const int w0 = min(nwords, t * per), w1 = min(nwords, w0 + per);
-    int mine = 0;
-    for (int i = w0; i < w1; ++i) mine += __popc(__ldcg(maskw + i));
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    named_sync(1, 128);
-    int before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        before += w < warp ? wsum[w] : 0;
-        total += wsum[w];
-    }
-    int off = before + incl - mine;
-    for (int i = w0; i < w1; ++i) {
-        uint32_t m = __ldcg(maskw + i);
-        while (m) {
-            const int bit = __ffs(m) - 1;
-            idx[off++] = i * 32 + bit;
-            m &= m - 1;
-        }
-    }
-    if (t == 0) *count = total;
-    named_sync(1, 128);
-}
-
 // Ticket on a tile counter: release this CTA's partial (written before the caller's
 // CTA-level barrier), and acquire everyone else's when the returned value completes the tile.
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v)
@@ -166,6 +130,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
     const uint32_t tmem = tmem_base;
 
     pdl_launch_dependents();
+    // Weight rows that do not depend on the previous kernel (the predictor's: no list, no
+    // count) are requested for the ring's first steps before waiting for that kernel, so their
+    // latency overlaps its tail; the activation tiles follow after the wait.
+    constexpr bool PRE_OK = MODE == TC_PRED_HIDDEN || MODE == TC_LOGITS;
+    const bool pre = PRE_OK && a.count == nullptr && a.idx == nullptr;
+    uint32_t npre = 0;
+    if constexpr (PRE_OK) {
+        if (pre && warp >= 4 && warp < TC_MMA_WARP) {
+            const int p = threadIdx.x - 128;
+            const int tiles0 = (a.n_static + 127) / 128, KB0 = a.K / (64 * KW);
+            const long long T0 = (long long)tiles0 * KB0;
+            const long long b0 = T0 ? tc_begin(blockIdx.x, T0, gridDim.x) : 0;
+            const long long e0 = T0 ? tc_begin(blockIdx.x + 1, T0, gridDim.x) : 0;
+            for (long long it = b0; it < e0 && npre < (uint32_t)S; ++it, ++npre) {
+                const int t = (int)(it / KB0), kb = (int)(it - (long long)t * KB0);
+                const uint32_t st = sbase + npre * STAGE;
+#pragma unroll
+                for (int i = 0; i < CH; ++i) {
+                    const int c = p + TC_PROD * i;
+                    const int j = t * 128 + (c >> 3);
+                    if (c >= 1024) continue;
+                    const bool ok = j < a.n_static;
+                    const uint16_t *src = a.w0 + (size_t)(ok ? j : 0) * a.K + (c & 7) * 8;
+#pragma unroll
+                    for (int w = 0; w < KW; ++w)
+                        cp_async16(st + w * BLK + sw128_off(c >> 3, c & 7), src + (kb * KW + w) * 64, ok ? 16u : 0u);
+                }
+            }
+        }
+    }
     pdl_wait();
 
     // ---- problem size and this CTA's stream-K range
@@ -234,6 +228,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                         break;
                     }
                     const uint32_t st = sbase + (uint32_t)slot * STAGE;
+                    const bool need_a = q >= npre;   // the first npre steps' rows were requested before the wait
 #pragma unroll
                     for (int w = 0; w < KW; ++w) {
                         const int k0 = (kb * KW + w) * 64;
@@ -242,7 +237,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
 #pragma unroll
                             for (int i = 0; i < CH; ++i) {
                                 const int c = p + TC_PROD * i;
-                                if (c < 1024) {
+                                if (c < 1024 && need_a) {
                                     const uint16_t *src = rp[m][i];
                                     cp_async16(st + (m * KW + w) * BLK + sw128_off(c >> 3, c & 7), src ? src + k0 : W0,
                                                src ? 16u : 0u);
@@ -508,7 +503,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                     if (threadIdx.x == 0) s_last = atom_add_acq_rel(a.done_cnt, 1u) == (unsigned)tiles - 1;
                     named_sync(1, 128);
                     if (s_last) {
-                        tc_compact(a.maskw, nwords, a.idx_out, a.count_out, s_wsum);
+                        compact_words<4>(a.maskw, nwords, a.idx_out, a.count_out, s_wsum,
+                                         [] { named_sync(1, 128); });
                         if (threadIdx.x == 0) *a.done_cnt = 0u;
                     }
                 }
