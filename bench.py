@@ -270,6 +270,8 @@ def workload_of(args):
     w = WORKLOADS[args.workload]
     if args.layers:
         w = dataclasses.replace(w, n_layers=min(args.layers, w.n_layers))
+    if args.rank:
+        w = dataclasses.replace(w, r=args.rank)   # same FFN weights (streams are keyed by workload id)
     return w
 
 
@@ -401,6 +403,9 @@ def run_ours(args):
         "hbm_frac": hbm_gbs / peak,
         "bytes_per_step": bytes_per_step,
         "mean_active_per_layer": mean_count,
+        "predictor_byte_share": predictor_bytes(w) * w.n_layers / bytes_per_step if bytes_per_step else None,
+        "predictor_time_share": ((kinds.get("pred_hidden", (0.0, 0))[0] + kinds.get("pred_logits", (0.0, 0))[0]) /
+                                 sum(v[0] for v in kinds.values())) if ("pred_hidden" in kinds) else None,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w, dom), "algorithmic_bytes": dom_bytes,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
@@ -478,6 +483,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=None,
                     help="use only the first L layers (small-footprint profiling runs; default: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rank", type=int, default=None,
+                    help="predictor rank r instead of the workload's (the predictor-rank sweep)")
     ap.add_argument("--hot-fraction", type=float, default=0.0,
                     help="neurons that fired on at least this fraction of the profiling tokens have their rows "
                          "requested a layer ahead (batch 1); 0 (default) turns that off. The output does not "

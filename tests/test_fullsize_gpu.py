@@ -85,3 +85,40 @@ def test_benchmark_stack_end_to_end(P):
     assert compared >= 1
     assert ffn.status() == 0
     ffn.close()
+
+
+@pytest.mark.parametrize("r", [128, 256, 512])
+def test_predictor_rank_sweep_full_size(P, r):
+    """The predictor ranks of the rank sweep, at the benchmark workload's full d and f, layer 0."""
+    import dataclasses
+
+    w = dataclasses.replace(WORKLOADS["relullama7b_d4096_f11008_bf16_L32"], r=r)
+    (Lg, Lo), = build_layers(w, [0])
+    ffn = P.SparseFFN.from_workload(w, [Lg], max_batch=1)
+    u = rms_inputs(w, 1, seed=9)[0]
+    idx, cnt = ffn.predict(0, to_dev(u))
+    torch.cuda.synchronize()
+    gi = idx[: int(cnt.item())].cpu().numpy()
+    pr = oracle.predict(u.astype(np.float64), Lo["p1_t"], Lo["p2_t"], Lo["b_pred"], w.pdtype)
+    diff = np.setxor1d(gi, pr["idx"])
+    assert np.all(band_mask(pr["z"])[diff]), f"{diff.size} out-of-band mismatches"
+    # and one decode step through the persistent kernel of a 2-layer stack at this rank
+    w2 = dataclasses.replace(w, n_layers=2)
+    layers = build_layers(w2, range(2))
+    ffn2 = P.SparseFFN.from_workload(w2, [g for g, _ in layers], max_batch=1)
+    X = make_inputs(w2, 1, 1, seed=21, device="cpu").numpy()
+    counts = torch.zeros(2, dtype=torch.int32, device="cuda")
+    idx_out = torch.zeros((2, w2.f), dtype=torch.int32, device="cuda")
+    xo = ffn2.decode_stack(to_dev(X[0]), counts=counts, idx_out=idx_out)
+    torch.cuda.synchronize()
+    st = oracle.stack(X[0].astype(np.float64), [o for _, o in layers], w2.kind, w2.wdtype, w2.pdtype)
+    cg, ig = counts.cpu().numpy(), idx_out.cpu().numpy()
+    same = all(np.array_equal(ig[l, : cg[l]], st["idx"][l]) for l in range(2))
+    for l in range(2):
+        dl = np.setxor1d(ig[l, : cg[l]], st["idx"][l])
+        assert np.all(st["zmin"][l][dl] < oracle.BAND), (l, dl)
+    if same:
+        assert rel_l2(xo.cpu().numpy() - X[0], st["x_out"] - X[0]) <= TOL[w2.wdtype]
+    assert ffn.status() == 0 and ffn2.status() == 0
+    ffn.close()
+    ffn2.close()
