@@ -18,6 +18,10 @@ Steps, as the pages give them ("PowerInfer" paper walk-through page):
                                                             -> ``hot_first_order``
   * layers chained by a parameter-free RMS pre-norm residual (the pages are
     silent about non-FFN layers; this is the reading used)  -> ``stack``
+  * hot prefix (walk-through page, hot/cold neurons: a small set fires on most
+    inputs; summary page, Methodology): with ``hot_prefix = H`` the neurons
+    [0, H) of the hot-first order are active on every token and the
+    predictor decides only [H, f)                           -> ``predict``
 """
 from __future__ import annotations
 
@@ -106,8 +110,12 @@ def _u64(u) -> np.ndarray:
     return u.reshape(1, -1) if u.ndim == 1 else u
 
 
-def predict(u, p1_t, p2_t, b_pred, pdtype: str, tau: float = 0.0) -> dict:
-    """Predictor hidden layer, logits, union mask and ascending active indices."""
+def predict(u, p1_t, p2_t, b_pred, pdtype: str, tau: float = 0.0, hot_prefix: int = 0) -> dict:
+    """Predictor hidden layer, logits, union mask and ascending active indices.
+
+    hot_prefix = H > 0: neurons [0, H) are active without a predictor decision; their
+    entries of z are returned as +inf (no logit decides them, so none lies in a band).
+    """
     u = _u64(u)
     B, d = u.shape
     p1, p2 = raw(p1_t), raw(p2_t)
@@ -120,7 +128,15 @@ def predict(u, p1_t, p2_t, b_pred, pdtype: str, tau: float = 0.0) -> dict:
     idx = np.empty(f, np.int32)
     n = lib().orc_predict(_ptr(u), B, d, r, f, DT[pdtype], _ptr(p1), _ptr(p2), _ptr(bp), tau,
                           _ptr(hp), _ptr(z), _ptr(mask), _ptr(idx))
-    return {"hp": hp, "z": z, "mask": mask.astype(bool), "idx": idx[:n].copy(), "count": int(n)}
+    mask = mask.astype(bool)
+    idx = idx[:n].copy()
+    if hot_prefix > 0:
+        H = min(int(hot_prefix), f)
+        mask[:H] = True
+        z[:, :H] = np.inf
+        idx = np.flatnonzero(mask).astype(np.int32)
+        n = idx.size
+    return {"hp": hp, "z": z, "mask": mask, "idx": idx, "count": int(n)}
 
 
 def _ffn_args(layer: dict):
@@ -173,9 +189,10 @@ def hot_first_order(counts) -> np.ndarray:
     return perm
 
 
-def layer_forward(u, layer: dict, kind: str, wdtype: str, pdtype: str, tau: float = 0.0) -> dict:
+def layer_forward(u, layer: dict, kind: str, wdtype: str, pdtype: str, tau: float = 0.0,
+                  hot_prefix: int = 0) -> dict:
     """One layer: predict on u, then the sparse FFN over the predicted set."""
-    pr = predict(u, layer["p1_t"], layer["p2_t"], layer.get("b_pred"), pdtype, tau)
+    pr = predict(u, layer["p1_t"], layer["p2_t"], layer.get("b_pred"), pdtype, tau, hot_prefix)
     h, y = sparse_ffn(u, layer, pr["idx"], kind, wdtype)
     pr["h"], pr["y"] = h, y
     pr["zmin"] = np.abs(pr["z"]).min(axis=0) if pr["z"].size else np.zeros(0)
@@ -183,7 +200,7 @@ def layer_forward(u, layer: dict, kind: str, wdtype: str, pdtype: str, tau: floa
 
 
 def stack(x0, layers, kind: str, wdtype: str, pdtype: str, tau: float = 0.0, eps: float = RMS_EPS,
-          keep: bool = False) -> dict:
+          keep: bool = False, hot_prefix: int = 0) -> dict:
     """x_{l+1} = x_l + FFN_l(u_l), u_l = rms_norm(x_l); returns x_L and per-layer traces.
 
     `layers` is a sequence of layer dicts or a callable layer_index -> layer dict.
@@ -201,7 +218,7 @@ def stack(x0, layers, kind: str, wdtype: str, pdtype: str, tau: float = 0.0, eps
         if layer is None:
             break
         u = rms_norm(x, eps)
-        out = layer_forward(u, layer, kind, wdtype, pdtype, tau)
+        out = layer_forward(u, layer, kind, wdtype, pdtype, tau, hot_prefix)
         trace["idx"].append(out["idx"])
         trace["count"].append(out["count"])
         trace["zmin"].append(out["zmin"])

@@ -319,3 +319,37 @@ def test_stack_reduces_to_layers():
 
 def brute_rms(x, eps=1e-6):
     return x / np.sqrt((x * x).mean(axis=1, keepdims=True) + eps)
+
+
+@pytest.mark.parametrize("kind,wdt,pdt", [("gated", "bf16", "bf16"), ("relu", "f16", "f16")])
+def test_hot_prefix_mode(kind, wdt, pdt):
+    """Hot prefix H: neurons [0, H) always active, the predictor decides the rest.
+
+    Pins: H = 0 is the plain predictor; H = f is the dense FFN (the FFN equation over
+    every neuron); any H agrees with brute force (mask = any_b(Z > 0) | i < H); and the
+    layer output is the dense one whenever the true set lies inside the hot prefix plus
+    the predicted tail."""
+    rng = np.random.default_rng(31)
+    d, f, r, B = 64, 150, 12, 3
+    L = rand_layer(rng, d, f, r, kind, wdt, pdt)
+    U = rng.standard_normal((B, d))
+    plain = oracle.predict(U, L["p1_t"], L["p2_t"], L["b_pred"], pdt)
+    zero = oracle.predict(U, L["p1_t"], L["p2_t"], L["b_pred"], pdt, hot_prefix=0)
+    assert np.array_equal(zero["idx"], plain["idx"])
+    _, Z, M = brute.predictor(U, L["p1_t"], L["p2_t"], L["b_pred"], pdt)
+    for H in (1, 37, 149):
+        pr = oracle.predict(U, L["p1_t"], L["p2_t"], L["b_pred"], pdt, hot_prefix=H)
+        want = M | (np.arange(f) < H)
+        assert np.array_equal(pr["mask"], want)
+        assert np.array_equal(pr["idx"], np.flatnonzero(want))
+        assert np.all(np.isinf(pr["z"][:, :H])) and np.array_equal(pr["z"][:, H:], plain["z"][:, H:])
+        out = oracle.layer_forward(U, L, kind, wdt, pdt, hot_prefix=H)
+        Y, _ = brute.ffn_masked(U, L, want, kind, wdt)
+        assert rel(out["y"], Y) < 1e-12
+    full = oracle.layer_forward(U, L, kind, wdt, pdt, hot_prefix=f)
+    assert full["count"] == f
+    assert rel(full["y"], oracle.dense_ffn(U, L, kind, wdt)) < 1e-13
+    # a hot prefix that covers every truly active neuron gives the dense output too
+    ts = np.flatnonzero(brute.true_set(U, L, wdt))
+    out = oracle.layer_forward(U, L, kind, wdt, pdt, hot_prefix=int(ts.max()) + 1)
+    assert rel(out["y"], oracle.dense_ffn(U, L, kind, wdt)) < 1e-13
