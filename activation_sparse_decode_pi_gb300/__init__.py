@@ -35,7 +35,7 @@ EXPORTS = (
     "pi_ffn_create", "pi_ffn_destroy", "pi_predict", "pi_sparse_ffn", "pi_decode_stack",
     "pi_hot_first_order", "pi_permute_rows", "pi_get_status", "pi_status_string", "pi_abi_version",
     "pi_profile_begin", "pi_profile_end", "pi_sparse_ffn_noalloc", "pi_selftest_grid_barrier",
-    "pi_selftest_umma", "pi_ffn_set_hot_neurons",
+    "pi_selftest_umma", "pi_ffn_set_hot_neurons", "pi_ffn_set_hot_prefix",
 )
 PI_NOALLOC_SCRATCH_BYTES = 16 << 20
 KERNEL_KINDS = ("rms", "pred_hidden", "pred_logits", "ffn_h", "ffn_down", "reduce", "decode_stack")
@@ -82,6 +82,8 @@ _lib.pi_sparse_ffn_noalloc.argtypes = [ctypes.POINTER(PiFfnDesc), ctypes.POINTER
                                        _P, _P, _P]
 _lib.pi_selftest_grid_barrier.restype = ctypes.c_int
 _lib.pi_selftest_grid_barrier.argtypes = [_P, _I32, _P]
+_lib.pi_ffn_set_hot_prefix.restype = ctypes.c_int
+_lib.pi_ffn_set_hot_prefix.argtypes = [_P, _I32]
 _lib.pi_ffn_set_hot_neurons.restype = ctypes.c_int
 _lib.pi_ffn_set_hot_neurons.argtypes = [_P, _I32]
 _lib.pi_selftest_umma.restype = ctypes.c_int
@@ -163,6 +165,10 @@ def pi_sparse_ffn_noalloc(desc, layer, u, B, idx, count, y, status=None, stream=
 
 def pi_selftest_grid_barrier(work, extra, stream=None) -> None:
     _check(_lib.pi_selftest_grid_barrier(_ptr(work), extra, _stream(stream)), "pi_selftest_grid_barrier")
+
+
+def pi_ffn_set_hot_prefix(h, hot_prefix) -> None:
+    _check(_lib.pi_ffn_set_hot_prefix(h, hot_prefix), "pi_ffn_set_hot_prefix")
 
 
 def pi_ffn_set_hot_neurons(h, n_hot) -> None:
@@ -285,6 +291,9 @@ class SparseFFN:
 
     def set_hot_neurons(self, n_hot: int) -> None:
         pi_ffn_set_hot_neurons(self.h, n_hot)
+
+    def set_hot_prefix(self, hot_prefix: int) -> None:
+        pi_ffn_set_hot_prefix(self.h, hot_prefix)
 
     def status(self) -> int:
         return pi_get_status(self.h)

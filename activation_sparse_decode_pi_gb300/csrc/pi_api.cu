@@ -131,6 +131,7 @@ struct pi_ffn {
     // persistent decode-step kernel (batch 1)
     bool stack_ok = false;
     int n_hot = 0;                     // neurons [0, n_hot) expected to fire on most tokens
+    int hot_prefix = 0;                // neurons [0, hot_prefix) computed on every token
     StackLayer *stack_layers = nullptr;
     uint32_t *stack_mask = nullptr;
     float *stack_sumsq = nullptr;
@@ -253,7 +254,7 @@ cudaError_t enqueue_predict(const pi_ffn_t *h, int layer, const float *x, const 
     ProfScope p(h, s, PI_K_PRED_LOGITS);
     return launch_pred_logits(
         mk(h, dim3((D.f + PRED_ROWS_LOGIT - 1) / PRED_ROWS_LOGIT), (size_t)bt2 * D.r * 4, s, pdl), D.pdtype, bt2,
-        w.p2_t, D.r, D.f, w.b_pred, D.tau_logit, h->hp, B, h->maskw, h->tickets + 0, idx, count);
+        w.p2_t, D.r, D.f, w.b_pred, D.tau_logit, h->hp, B, h->maskw, h->tickets + 0, idx, count, h->hot_prefix);
 }
 
 // K3 + K4a + K4b for one layer. xin != NULL: stack glue (out = xin + y, inv_rms for the next layer).
@@ -431,8 +432,11 @@ cudaError_t tc_predict(const pi_ffn_t *h, int layer, int B, int32_t *idx, int32_
     }
     if (e != cudaSuccess) return e;
     TcArgs a = tc_args();
+    // the tiles start at the last 128-row boundary inside the hot prefix (keeping one tile)
+    a.hot = h->hot_prefix;
+    a.row0 = std::min(h->hot_prefix / 128, (D.f - 1) / 128) * 128;
     a.w0 = (const uint16_t *)w.p2_t;
-    a.n_static = D.f;
+    a.n_static = D.f - a.row0;
     a.f = D.f;
     a.K = D.r;
     a.d = D.d;
@@ -631,6 +635,7 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.off_flags = h->off_flags;
     a.off_mbar = h->off_mbar;
     a.ring_bytes = h->stack_ring;
+    a.hot_prefix = h->hot_prefix;
     a.hot_k = h->n_hot > 0 ? std::min((h->n_hot + h->nsm - 1) / h->nsm, h->stack_slots - 2) : 0;
     if (a.hot_k < 0) a.hot_k = 0;
     a.bias_bulk = D.f % 4 == 0 ? 1 : 0;
@@ -877,6 +882,13 @@ pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_ou
         h->g_idx = idx_out;
     }
     return cuda_status(cudaGraphLaunch(h->gexec, st));
+}
+
+pi_status_t pi_ffn_set_hot_prefix(pi_ffn_t *h, int32_t n_hot)
+{
+    if (!h || n_hot < 0 || n_hot > h->desc.f) return PI_ERR_INVALID_ARG;
+    h->hot_prefix = n_hot;
+    return PI_OK;
 }
 
 pi_status_t pi_ffn_set_hot_neurons(pi_ffn_t *h, int32_t n_hot)

@@ -125,20 +125,23 @@ __device__ __forceinline__ int warp_sum_int(int v)
     return v;
 }
 
-// Ascending list of the set bits of maskw[0..nwords) (bit b of word w = neuron 32 w + b)
-// into idx, and their number into *count, by NWARPS warps; `sync` is a barrier over
+// Ascending list of the set bits of maskw[0..nwords) (bit b of word w = neuron 32 w + b;
+// the first `full` words are taken as all ones without being read) into idx, and their
+// number into *count, by NWARPS warps; `sync` is a barrier over
 // exactly those warps, wsum NWARPS ints of shared memory. Warp g takes a contiguous block of
 // words, loads them 32 at a time (one coalesced load) and emits each word's set bits to
 // consecutive entries in one coalesced store.
 template <int NWARPS, typename Sync>
-__device__ __forceinline__ void compact_words(const uint32_t *__restrict__ maskw, int nwords, int32_t *__restrict__ idx,
-                                              int32_t *__restrict__ count, int *wsum, Sync sync)
+__device__ __forceinline__ void compact_words(const uint32_t *__restrict__ maskw, int nwords, int full,
+                                              int32_t *__restrict__ idx, int32_t *__restrict__ count, int *wsum,
+                                              Sync sync)
 {
     const int warp = (threadIdx.x >> 5) % NWARPS, lane = threadIdx.x & 31;
     const int wpw = (nwords + NWARPS - 1) / NWARPS;
     const int wb = min(nwords, warp * wpw), we = min(nwords, wb + wpw);
     int cnt = 0;
-    for (int b = wb; b < we; b += 32) cnt += __popc(b + lane < we ? __ldcg(maskw + b + lane) : 0u);
+    auto word = [&](int w) -> uint32_t { return w < full ? 0xffffffffu : __ldcg(maskw + w); };
+    for (int b = wb; b < we; b += 32) cnt += __popc(b + lane < we ? word(b + lane) : 0u);
     cnt = warp_sum_int(cnt);
     if (lane == 0) wsum[warp] = cnt;
     sync();
@@ -150,7 +153,7 @@ __device__ __forceinline__ void compact_words(const uint32_t *__restrict__ maskw
     }
     const uint32_t below = (1u << lane) - 1u;
     for (int b = wb; b < we; b += 32) {
-        const uint32_t mine = b + lane < we ? __ldcg(maskw + b + lane) : 0u;
+        const uint32_t mine = b + lane < we ? word(b + lane) : 0u;
         const int nk = min(32, we - b);
         for (int k = 0; k < nk; ++k) {
             const uint32_t m = __shfl_sync(0xffffffffu, mine, k);

@@ -53,6 +53,7 @@ struct StackArgs {
     int ring_bytes;               // ring region: the neuron slots
     int bias_bulk;                // gate biases ride in the row copies (every layer has one and f % 4 == 0)
     int hot_k;                    // ring slots per CTA held by hot owned neurons (loaded a layer ahead), <= slots - 2
+    int hot_prefix;               // neurons below this are active without a logit
 };
 
 template <int WT>
@@ -76,6 +77,8 @@ struct TcArgs {
     int ldx, B;
     const float *bias;            // per-row bias indexed by row id, or NULL
     float tau;
+    int row0;                     // row id of row 0 when there is no list (TC_LOGITS: start of the tiles)
+    int hot;                      // TC_LOGITS: row ids below this are active without a logit (hot prefix)
     uint16_t *ohi, *olo;          // outputs hi/lo [NB x ldo] (hidden / h)
     int ldo;
     uint32_t *maskw;              // TC_LOGITS: mask words, then ascending idx_out, count_out
@@ -116,11 +119,12 @@ struct Launch {
 cudaError_t launch_pred_hidden(const Launch &L, int pdt, int bt, const void *p1t, int d, int r,
                                const float *x, const float *inv_rms, int B, float *hp);
 
-// K2: z = hp . p2_t[i] + b_pred[i]; mask bit i = OR_b (z > tau); the last CTA compacts
-// the mask words into ascending idx[] and *count. ticket must be 0 on entry (left 0).
+// K2: z = hp . p2_t[i] + b_pred[i]; mask bit i = OR_b (z > tau), and 1 without a logit for
+// i < hot (hot prefix); the last CTA compacts the mask words into ascending idx[] and *count.
+// ticket must be 0 on entry (left 0).
 cudaError_t launch_pred_logits(const Launch &L, int pdt, int bt, const void *p2t, int r, int f,
                                const float *b_pred, float tau, const float *hp, int B,
-                               uint32_t *maskw, uint32_t *ticket, int32_t *idx, int32_t *count);
+                               uint32_t *maskw, uint32_t *ticket, int32_t *idx, int32_t *count, int hot);
 
 // K3: h[b,j] for the listed neurons j < *count.
 cudaError_t launch_ffn_h(const Launch &L, int wdt, int kind, int bt, const void *wg, const void *wu,

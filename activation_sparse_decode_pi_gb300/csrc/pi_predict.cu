@@ -87,7 +87,7 @@ template <int PT, int BT>
 __global__ void __launch_bounds__(NT, 2)
 k_pred_logits(const uint4 *__restrict__ P2, int r, int f, const float *__restrict__ b_pred, float tau,
               const float *__restrict__ hp, int B, uint32_t *__restrict__ maskw, uint32_t *__restrict__ ticket,
-              int32_t *__restrict__ idx, int32_t *__restrict__ count)
+              int32_t *__restrict__ idx, int32_t *__restrict__ count, int hot)
 {
     constexpr int RW = PRED_ROWS_LOGIT / NW, U = 4, V = Vec<PT>::N;
     extern __shared__ float4 su4[];                 // [BT][r/4] planar
@@ -103,7 +103,7 @@ k_pred_logits(const uint4 *__restrict__ P2, int r, int f, const float *__restric
 #pragma unroll
     for (int k = 0; k < RW; ++k) {
         const int i = n0 + warp + NW * k;
-        row[k] = i < f ? P2 + (size_t)i * nch : nullptr;
+        row[k] = (i < f && i >= hot) ? P2 + (size_t)i * nch : nullptr;   // hot prefix: no logit needed
         srow[k] = nullptr;
     }
     if (threadIdx.x == 0) word = 0u;
@@ -138,7 +138,7 @@ k_pred_logits(const uint4 *__restrict__ P2, int r, int f, const float *__restric
 #pragma unroll
             for (int b = 0; b < BT; ++b) {
                 const float z = warp_sum(acc[k][b]) + bias;
-                if (i < f && b < bt && z > tau) bits |= 1u << (warp + NW * k);
+                if (i < f && b < bt && (i < hot || z > tau)) bits |= 1u << (warp + NW * k);
             }
         }
     }
@@ -153,7 +153,7 @@ k_pred_logits(const uint4 *__restrict__ P2, int r, int f, const float *__restric
     if (!last) return;
     __threadfence();
     __shared__ int wsum[NW];
-    compact_words<NW>(maskw, gridDim.x, idx, count, wsum, [] { __syncthreads(); });
+    compact_words<NW>(maskw, gridDim.x, 0, idx, count, wsum, [] { __syncthreads(); });
     if (threadIdx.x == 0) *ticket = 0u;
 }
 
@@ -190,13 +190,13 @@ cudaError_t launch_pred_hidden(const Launch &L, int pdt, int bt, const void *p1t
 template <int PT>
 static cudaError_t logits_bt(const Launch &L, int bt, const void *p2t, int r, int f, const float *b_pred,
                              float tau, const float *hp, int B, uint32_t *maskw, uint32_t *ticket,
-                             int32_t *idx, int32_t *count)
+                             int32_t *idx, int32_t *count, int hot)
 {
     auto go = [&](auto kern) {
         cudaError_t e = ensure_smem(kern, L.smem);
         return e != cudaSuccess ? e
                                 : launch_ex(L, kern, (const uint4 *)p2t, r, f, b_pred, tau, hp, B, maskw, ticket,
-                                            idx, count);
+                                            idx, count, hot);
     };
     switch (bt) {
     case 1: return go(k_pred_logits<PT, 1>);
@@ -209,12 +209,12 @@ static cudaError_t logits_bt(const Launch &L, int bt, const void *p2t, int r, in
 
 cudaError_t launch_pred_logits(const Launch &L, int pdt, int bt, const void *p2t, int r, int f,
                                const float *b_pred, float tau, const float *hp, int B,
-                               uint32_t *maskw, uint32_t *ticket, int32_t *idx, int32_t *count)
+                               uint32_t *maskw, uint32_t *ticket, int32_t *idx, int32_t *count, int hot)
 {
     switch (pdt) {
-    case DT_F32: return logits_bt<DT_F32>(L, bt, p2t, r, f, b_pred, tau, hp, B, maskw, ticket, idx, count);
-    case DT_BF16: return logits_bt<DT_BF16>(L, bt, p2t, r, f, b_pred, tau, hp, B, maskw, ticket, idx, count);
-    case DT_F16: return logits_bt<DT_F16>(L, bt, p2t, r, f, b_pred, tau, hp, B, maskw, ticket, idx, count);
+    case DT_F32: return logits_bt<DT_F32>(L, bt, p2t, r, f, b_pred, tau, hp, B, maskw, ticket, idx, count, hot);
+    case DT_BF16: return logits_bt<DT_BF16>(L, bt, p2t, r, f, b_pred, tau, hp, B, maskw, ticket, idx, count, hot);
+    case DT_F16: return logits_bt<DT_F16>(L, bt, p2t, r, f, b_pred, tau, hp, B, maskw, ticket, idx, count, hot);
     }
     return cudaErrorInvalidValue;
 }

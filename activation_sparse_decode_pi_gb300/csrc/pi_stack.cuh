@@ -63,15 +63,17 @@ __device__ __forceinline__ void load_p1_chunk(RowChunks<PT, 8, 1> &pa, const voi
     rows_issue(pa, row, srow, c, ce);
 }
 
-// Rows kbase, kbase + step, ... of the neurons a CTA owns (i = c + P * k, k < K) in a [f x r] matrix.
+// Rows kbase, kbase + step, ... of the neurons a CTA owns (i = c + P * k, k < K) in a [f x r] matrix;
+// none for neurons below `hot` (the hot prefix needs no logit).
 template <int RW>
 __device__ __forceinline__ void owned_rows(const uint4 *(&row)[RW], const void *m, int kbase, int step, int K, int c,
-                                           int P, int nch)
+                                           int P, int nch, int hot)
 {
 #pragma unroll
     for (int q = 0; q < RW; ++q) {
         const int k = kbase + step * q;
-        row[q] = k < K ? reinterpret_cast<const uint4 *>(m) + (size_t)(c + (size_t)P * k) * nch : nullptr;
+        const int i = c + P * k;
+        row[q] = (k < K && i >= hot) ? reinterpret_cast<const uint4 *>(m) + (size_t)i * nch : nullptr;
     }
 }
 
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 const int t = tid + u * STACK_NT;
                 hv[u] = t < r4 ? __ldcg(reinterpret_cast<const float4 *>(a.hp) + t) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            owned_rows<5>(row, Lw.p2, warp, SNW, K, c, P, nchr);
+            owned_rows<5>(row, Lw.p2, warp, SNW, K, c, P, nchr, a.hot_prefix);
             rows_issue(rc, row, srow, lane, nchr);                  // before hp is staged
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             __syncthreads();
             for (int kbase = warp; kbase < K; kbase += SNW * 5) {
                 if (kbase != warp) {
-                    owned_rows<5>(row, Lw.p2, kbase, SNW, K, c, P, nchr);
+                    owned_rows<5>(row, Lw.p2, kbase, SNW, K, c, P, nchr, a.hot_prefix);
                     rows_issue(rc, row, srow, lane, nchr);
                 }
                 float acc[5][1] = {{0.f}, {0.f}, {0.f}, {0.f}, {0.f}};
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     const int k = kbase + SNW * q;
                     const int i = c + P * k;
                     const float z = warp_sum(acc[q][0]) + ((k < K && Lw.bp) ? __ldg(Lw.bp + i) : 0.f);
-                    if (lane == 0 && k < K) sflag[k] = z > a.tau ? 1 : 0;
+                    if (lane == 0 && k < K) sflag[k] = (i < a.hot_prefix || z > a.tau) ? 1 : 0;
                 }
             }
             __syncthreads();

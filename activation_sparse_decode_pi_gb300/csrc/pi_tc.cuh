@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                     const int j = t * 128 + (c >> 3);
                     if (c >= 1024) continue;
                     const bool ok = j < a.n_static;
-                    const uint16_t *src = a.w0 + (size_t)(ok ? j : 0) * a.K + (c & 7) * 8;
+                    const uint16_t *src = a.w0 + (size_t)(ok ? a.row0 + j : 0) * a.K + (c & 7) * 8;
 #pragma unroll
                     for (int w = 0; w < KW; ++w)
                         cp_async16(st + w * BLK + sw128_off(c >> 3, c & 7), src + (kb * KW + w) * 64, ok ? 16u : 0u);
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                     const int j = t * 128 + (c >> 3);
                     int id = -1;
                     if (c < 1024 && j < n) {
-                        id = a.idx ? __ldcg(a.idx + j) : j;
+                        id = a.idx ? __ldcg(a.idx + j) : a.row0 + j;
                         if (id < 0 || id >= a.f) {
                             bad = true;
                             id = -1;
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                 if constexpr (!DOWN) {
                     const int j = t * 128 + m;
                     if (j < n) {
-                        id = a.idx ? __ldcg(a.idx + j) : j;
+                        id = a.idx ? __ldcg(a.idx + j) : a.row0 + j;
                         if (id < 0 || id >= a.f) id = -1;
                     }
                 }
@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                                 }
                             }
                         } else if constexpr (MODE == TC_LOGITS) {
-                            act |= id >= 0 && b < a.B && (v[0][i] + bias > a.tau);
+                            act |= id >= 0 && b < a.B && (id < a.hot || v[0][i] + bias > a.tau);
                         } else {
                             const int j = t * 128 + m;
                             float hv = 0.f;
@@ -497,13 +497,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                 }
                 if constexpr (MODE == TC_LOGITS) {
                     const uint32_t word = __ballot_sync(0xffffffffu, act);
-                    const int wi = (t * 128 + 32 * warp) >> 5;
+                    const int wi = (a.row0 + t * 128 + 32 * warp) >> 5;
                     if (lane == 0 && wi < nwords) a.maskw[wi] = word;
                     named_sync(1, 128);
                     if (threadIdx.x == 0) s_last = atom_add_acq_rel(a.done_cnt, 1u) == (unsigned)tiles - 1;
                     named_sync(1, 128);
                     if (s_last) {
-                        compact_words<4>(a.maskw, nwords, a.idx_out, a.count_out, s_wsum,
+                        compact_words<4>(a.maskw, nwords, a.row0 / 32, a.idx_out, a.count_out, s_wsum,
                                          [] { named_sync(1, 128); });
                         if (threadIdx.x == 0) *a.done_cnt = 0u;
                     }

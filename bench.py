@@ -104,10 +104,10 @@ def barrier(world: int):
 # bytes
 # ------------------------------------------------------------------------------------------------
 
-def predictor_bytes(w) -> float:
-    """Dense predictor weights plus its fp32 bias, per layer."""
+def predictor_bytes(w, hot: int = 0) -> float:
+    """Predictor weights plus its fp32 bias, per layer (the hot prefix's P2 rows are not read)."""
     pb = WB[w.pdtype]
-    return w.r * w.d * pb + w.f * w.r * pb + w.f * 4
+    return w.r * w.d * pb + (w.f - hot) * w.r * pb + w.f * 4
 
 
 def neuron_bytes(w) -> float:
@@ -119,20 +119,20 @@ def neuron_bytes(w) -> float:
     return b
 
 
-def step_bytes(w, counts_per_layer) -> float:
-    return float(sum(predictor_bytes(w) + c * neuron_bytes(w) for c in counts_per_layer))
+def step_bytes(w, counts_per_layer, hot: int = 0) -> float:
+    return float(sum(predictor_bytes(w, hot) + c * neuron_bytes(w) for c in counts_per_layer))
 
 
-def kernel_bytes(w, kind: str, count: float, B: int, counts_per_layer=None) -> float:
+def kernel_bytes(w, kind: str, count: float, B: int, counts_per_layer=None, hot: int = 0) -> float:
     """Algorithmic HBM bytes of one launch of a kernel kind (weights it must read once)."""
     if kind == "decode_stack":   # one launch = one whole decode step
-        return step_bytes(w, counts_per_layer if counts_per_layer is not None else [count] * w.n_layers)
+        return step_bytes(w, counts_per_layer if counts_per_layer is not None else [count] * w.n_layers, hot)
     pb, wb = WB[w.pdtype], WB[w.wdtype]
     sc = (w.d // 128) * 2 if w.wdtype == "int4g128" else 0
     if kind == "pred_hidden":
         return w.r * w.d * pb
     if kind == "pred_logits":
-        return w.f * w.r * pb + w.f * 4
+        return (w.f - hot) * w.r * pb + w.f * 4
     if kind == "ffn_h":
         rows = 2 if w.kind == "gated" else 1
         return count * (rows * (w.d * wb + sc) + 4)
@@ -216,25 +216,31 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def build_model(w, device, hot_fraction: float = 0.0):
-    """Layers in hot-first order, and the number of leading neurons that fired on at least
-    `hot_fraction` of the profiling tokens in every layer (0 when hot_fraction <= 0)."""
-    import activation_sparse_decode_pi_gb300 as P
+def hot_count(counts, fraction: float) -> int:
+    """Leading neurons (hot-first order) that fired on at least `fraction` of the profiling
+    tokens in every layer: the offline profile's hot set (0 when fraction <= 0)."""
     from workload.gen import T_CALIB
 
-    layers, n_hot = [], w.f
+    if fraction <= 0 or not counts:
+        return 0
+    return min(int((c >= fraction * T_CALIB).sum().item()) for c in counts)
+
+
+def build_model(w, device):
+    """Layers in hot-first order, and each layer's profiling counts in that order."""
+    import activation_sparse_decode_pi_gb300 as P
+
+    layers, counts = [], []
     for l in range(w.n_layers):
         L = make_layer(w, l, 0, device=device)
         Lg, _ = P.apply_hot_first(L)
-        if hot_fraction > 0:
-            n_hot = min(n_hot, int((Lg["counts"] >= hot_fraction * T_CALIB).sum().item()))
-        for k in ("p", "counts"):
-            Lg.pop(k, None)
+        counts.append(Lg.pop("counts").cpu())
+        Lg.pop("p", None)
         layers.append(Lg)
         del L
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
-    return layers, (n_hot if hot_fraction > 0 else 0)
+    return layers, counts
 
 
 def cpu_baseline(w, B, seconds: float = 15.0, max_tokens: int = 64):
@@ -287,9 +293,11 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     w = workload_of(args)
     B = args.batch
-    layers, n_hot = build_model(w, dev, args.hot_fraction)
+    layers, counts_l = build_model(w, dev)
+    n_hot, hot_prefix = hot_count(counts_l, args.hot_fraction), hot_count(counts_l, args.hot_prefix_fraction)
     ffn = P.SparseFFN.from_workload(w, layers, max_batch=B)
     ffn.set_hot_neurons(n_hot)
+    ffn.set_hot_prefix(hot_prefix)
     X = make_inputs(w, POOL_TOKENS, B, seed=1000 + rank, device=dev).contiguous()
     x_in = torch.empty((B, w.d), dtype=torch.float32, device=dev)
     x_out = torch.empty((B, w.d), dtype=torch.float32, device=dev)
@@ -336,7 +344,7 @@ def run_ours(args):
     if per_step:
         cts = torch.stack(per_step).cpu().numpy().astype(np.float64)
     mean_counts = cts.mean(axis=0) if len(cts) else np.zeros(w.n_layers)
-    bytes_per_step = step_bytes(w, mean_counts)
+    bytes_per_step = step_bytes(w, mean_counts, hot_prefix)
     hbm_gbs = bytes_per_step * args.steps / (ms_local / 1e3) / 1e9
 
     # ---- per-kernel durations (events around each launch, no overlap) for the roofline
@@ -350,11 +358,11 @@ def run_ours(args):
     dom = max(kinds, key=lambda k: kinds[k][0])
     dom_ms, dom_n = kinds[dom]
     mean_count = float(mean_counts.mean()) if len(mean_counts) else 0.0
-    dom_bytes = kernel_bytes(w, dom, mean_count, B, mean_counts)
+    dom_bytes = kernel_bytes(w, dom, mean_count, B, mean_counts, hot_prefix)
     achieved = dom_bytes / (dom_ms / dom_n / 1e3) / 1e9
     kernel_table = {k: {"ms_per_launch": v[0] / v[1], "launches": v[1],
                         "share": v[0] / sum(x[0] for x in kinds.values()),
-                        "gbs": kernel_bytes(w, k, mean_count, B, mean_counts) / (v[0] / v[1] / 1e3) / 1e9}
+                        "gbs": kernel_bytes(w, k, mean_count, B, mean_counts, hot_prefix) / (v[0] / v[1] / 1e3) / 1e9}
                     for k, v in kinds.items()}
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
@@ -398,12 +406,12 @@ def run_ours(args):
                    "weights": w.wdtype, "predictor": w.pdtype, "batch": B, "global_batch": B * world,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {bytes_per_step / 1e9:.2f} GB of distinct weights per step",
-                   "hot_neurons": n_hot},
+                   "hot_neurons": n_hot, "hot_prefix": hot_prefix},
         "hbm_gbs": hbm_gbs,
         "hbm_frac": hbm_gbs / peak,
         "bytes_per_step": bytes_per_step,
         "mean_active_per_layer": mean_count,
-        "predictor_byte_share": predictor_bytes(w) * w.n_layers / bytes_per_step if bytes_per_step else None,
+        "predictor_byte_share": predictor_bytes(w, hot_prefix) * w.n_layers / bytes_per_step if bytes_per_step else None,
         "predictor_time_share": ((kinds.get("pred_hidden", (0.0, 0))[0] + kinds.get("pred_logits", (0.0, 0))[0]) /
                                  sum(v[0] for v in kinds.values())) if ("pred_hidden" in kinds) else None,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -483,6 +491,10 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=None,
                     help="use only the first L layers (small-footprint profiling runs; default: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--hot-prefix-fraction", type=float, default=0.0,
+                    help="the hot-prefix variant: neurons that fired on at least this fraction of the profiling "
+                         "tokens are computed on every token, the predictor decides the rest; 0 (default) is the "
+                         "plain method")
     ap.add_argument("--rank", type=int, default=None,
                     help="predictor rank r instead of the workload's (the predictor-rank sweep)")
     ap.add_argument("--hot-fraction", type=float, default=0.0,

@@ -245,6 +245,19 @@ pi_status_t pi_selftest_umma(const void *a, const void *b, float *d, int32_t mod
                              int32_t dtype, uint32_t *status, void *stream);
 
 /*
+ * Hot prefix (a variant of the method). The pages split neurons into hot ones, which fire on
+ * most inputs and are served without question, and cold ones, which the predictor decides
+ * ("PowerInfer" paper walk-through page, hot/cold neurons and inference flow; summary page,
+ * Methodology). With hot_prefix = H, neurons [0, H) of the hot-first order are active on
+ * every token without a logit (their P2 rows are not read), and the predictor decides only
+ * [H, f). pi_predict returns [0, H) followed by the predicted tail, ascending; pi_decode_stack
+ * computes both. The result differs from H = 0 only where the predictor would have dropped a
+ * hot neuron whose gate is positive: it is then closer to the dense FFN. 0 (the default) is
+ * the plain method. Returns PI_ERR_INVALID_ARG unless 0 <= H <= f. Takes effect from the next call.
+ */
+pi_status_t pi_ffn_set_hot_prefix(pi_ffn_t *h, int32_t hot_prefix);
+
+/*
  * Hot neurons of the batch-1 decode step. The offline profile ("PowerInfer" paper
  * walk-through, offline profiling code block; summary page, Methodology: a small set of
  * hot neurons fires on most inputs) orders neurons hot-first; n_hot says that neurons

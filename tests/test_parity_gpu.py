@@ -363,3 +363,63 @@ def test_decode_stack_hot_neurons_bit_identical(P, wi):
         ffn.set_hot_neurons(w.f + 1)
     assert ffn.status() == 0
     ffn.close()
+
+
+# ------------------------------------------------------------------ hot-prefix variant --------
+
+def _check_list(gi, pr, H):
+    assert np.all(np.diff(gi) > 0)
+    assert np.array_equal(gi[: min(H, gi.size)], np.arange(min(H, gi.size)))
+    diff = np.setxor1d(gi, pr["idx"])
+    assert np.all(band_mask(pr["z"])[diff]), f"{diff.size} out-of-band mismatches"
+
+
+@pytest.mark.parametrize("wi", range(5))
+def test_hot_prefix_predict_and_stack(P, wi):
+    """Neurons [0, H) active without a logit: pi_predict (batch 1 and 4) and both batch-1 stack
+    paths against the oracle's hot-prefix mode."""
+    w = _wl(wi, STACK_SHAPE, n_layers=2)
+    layers = build_layers(w, range(w.n_layers))
+    Lo0 = layers[0][1]
+    X = make_inputs(w, 2, 1, seed=17, device="cpu").numpy()
+    for H in (200, 1500, w.f):
+        for B in (1, 4):
+            ffn = P.SparseFFN.from_workload(w, [g for g, _ in layers], max_batch=B)
+            ffn.set_hot_prefix(H)
+            u = rms_inputs(w, B, seed=H)[0]
+            idx, cnt = ffn.predict(0, to_dev(u))
+            torch.cuda.synchronize()
+            gi = idx[: int(cnt.item())].cpu().numpy()
+            pr = oracle.predict(u.astype(np.float64), Lo0["p1_t"], Lo0["p2_t"], Lo0["b_pred"], w.pdtype, hot_prefix=H)
+            _check_list(gi, pr, H)
+            assert ffn.status() == 0
+            ffn.close()
+        for stack_kernel in (True, False):
+            ffn = _handle(P, w, [g for g, _ in layers], stack_kernel)
+            ffn.set_hot_prefix(H)
+            for t in range(X.shape[0]):
+                counts = torch.zeros(w.n_layers, dtype=torch.int32, device="cuda")
+                idx_out = torch.zeros((w.n_layers, w.f), dtype=torch.int32, device="cuda")
+                xo = ffn.decode_stack(to_dev(X[t]), counts=counts, idx_out=idx_out)
+                torch.cuda.synchronize()
+                st = oracle.stack(X[t].astype(np.float64), [o for _, o in layers], w.kind, w.wdtype, w.pdtype,
+                                  hot_prefix=H)
+                cg, ig = counts.cpu().numpy(), idx_out.cpu().numpy()
+                same = True
+                for l in range(w.n_layers):
+                    gi = ig[l, : cg[l]]
+                    assert np.array_equal(gi[: min(H, gi.size)], np.arange(min(H, gi.size)))
+                    diff = np.setxor1d(gi, st["idx"][l])
+                    if diff.size:
+                        assert np.all(st["zmin"][l][diff] < oracle.BAND), (stack_kernel, H, l, diff)
+                        same = False
+                        break
+                if same:
+                    err = rel_l2(xo.cpu().numpy() - X[t], st["x_out"] - X[t])
+                    assert err <= TOL[w.wdtype], (stack_kernel, H, err)
+            assert ffn.status() == 0
+            ffn.close()
+    ffn = P.SparseFFN.from_workload(w, [g for g, _ in layers], max_batch=1)
+    with pytest.raises(P.PiError):
+        ffn.set_hot_prefix(w.f + 1)
+    ffn.close()

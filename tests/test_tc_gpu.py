@@ -188,3 +188,25 @@ def test_tc_step_widths(P, kw, ds, wi, B):
     u, pr = _predict_check(P, ffn, w, Lo, B, seed=3 * B)
     _ffn_check(P, ffn, w, Lo, u, pr, seed=kw * 10 + ds)
     ffn.close()
+
+
+@pytest.mark.parametrize("H", [100, 128, 1000, 2999, 3001])
+@pytest.mark.parametrize("wi,B", [(2, 16), (3, 32)])
+def test_tc_hot_prefix(P, wi, B, H):
+    """Tensor-core logits with a hot prefix: the tiles start at the last 128-row boundary
+    inside it, the words below are all ones, the rows in between are forced active."""
+    w = scaled(W[wi], n_layers=1, **TC_SHAPES[0])
+    (Lg, Lo), = build_layers(w, [0])
+    ffn = _handle(P, w, [Lg], B)
+    ffn.set_hot_prefix(H)
+    u = rms_inputs(w, B, seed=H)[0]
+    idx, cnt = ffn.predict(0, to_dev(u))
+    torch.cuda.synchronize()
+    gi = idx[: int(cnt.item())].cpu().numpy()
+    pr = oracle.predict(u.astype(np.float64), Lo["p1_t"], Lo["p2_t"], Lo["b_pred"], w.pdtype, hot_prefix=H)
+    assert np.all(np.diff(gi) > 0)
+    assert np.array_equal(gi[:H], np.arange(H))
+    diff = np.setxor1d(gi, pr["idx"])
+    assert np.all(band_mask(pr["z"])[diff]), f"{diff.size} out-of-band mismatches"
+    assert ffn.status() == 0
+    ffn.close()
