@@ -42,29 +42,37 @@ CSRC = os.path.join(ROOT, "activation_sparse_decode_pi_gb300", "csrc")
 # dram__bytes_write.sum), with a hash of the kernel sources it was taken on. The capture ran a
 # 4-layer slice of the workload; traffic grows in proportion to layers, so it is kept per layer.
 # A source change makes the recorded figure stale and the bench then reports null.
+# DRAM bytes (read + write) per launch of a kernel, from one ncu capture, valid while the
+# sources that kernel is built from hash to the value recorded with it
+KERNEL_SOURCES = {
+    "decode_stack": ("pi_stack.cuh", "pi_stack_f32.cu", "pi_stack_bf16.cu", "pi_stack_f16.cu", "pi_stack_int4.cu",
+                     "pi_async.cuh", "pi_common.cuh", "pi_rowdot.cuh"),
+}
 NCU_TRAFFIC = {
-    ("relullama7b_d4096_f11008_bf16_L32", "decode_stack"): {"bytes_per_layer": 238313216 / 4,
-                                                            "csrc": "04668426e57d3363"},
+    # 4-layer slice: dram__bytes_read.sum 234.986496 MB + dram__bytes_write.sum 4.037888 MB
+    ("relullama7b_d4096_f11008_bf16_L32", "decode_stack"): {"bytes_per_layer": (234986496 + 4037888) / 4,
+                                                            "csrc": "38902b75946a8927"},
 }
 
 
-def csrc_hash() -> str:
+def csrc_hash(kernel: str) -> str:
     import hashlib
 
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            with open(os.path.join(CSRC, name), "rb") as fh:
-                h.update(fh.read())
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode())
+        with open(os.path.join(CSRC, name), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(w, kernel: str):
     rec = NCU_TRAFFIC.get((w.name, kernel))
-    if not rec or rec["csrc"] != csrc_hash():
+    if not rec or not rec["bytes_per_layer"] or kernel not in KERNEL_SOURCES or rec["csrc"] != csrc_hash(kernel):
         return None
     return rec["bytes_per_layer"] * w.n_layers
+
+
 METRIC = "sparse-FFN decode tokens/s (batch 1) and achieved HBM GB/s vs peak on GB300"
 POOL_TOKENS = 256
 WB = {"f32": 4.0, "bf16": 2.0, "f16": 2.0, "int4g128": 0.5}
