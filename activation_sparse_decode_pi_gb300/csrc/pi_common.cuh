@@ -127,21 +127,33 @@ __device__ __forceinline__ int warp_sum_int(int v)
 
 // Ascending list of the set bits of maskw[0..nwords) (bit b of word w = neuron 32 w + b;
 // the first `full` words are taken as all ones without being read) into idx, and their
-// number into *count, by NWARPS warps; `sync` is a barrier over
-// exactly those warps, wsum NWARPS ints of shared memory. Warp g takes a contiguous block of
-// words, loads them 32 at a time (one coalesced load) and emits each word's set bits to
-// consecutive entries in one coalesced store.
+// number into *count, by NWARPS warps; `sync` is a barrier over exactly those warps, wsum
+// NWARPS ints of shared memory. Warp g takes a contiguous block of words and reads it in
+// slabs of 32 * CW words, all loads of a slab in flight at once (one round trip to L2 per
+// slab); each word's set bits go to consecutive entries in one coalesced store.
 template <int NWARPS, typename Sync>
 __device__ __forceinline__ void compact_words(const uint32_t *__restrict__ maskw, int nwords, int full,
                                               int32_t *__restrict__ idx, int32_t *__restrict__ count, int *wsum,
                                               Sync sync)
 {
+    constexpr int CW = 8;   // words per lane per slab
     const int warp = (threadIdx.x >> 5) % NWARPS, lane = threadIdx.x & 31;
     const int wpw = (nwords + NWARPS - 1) / NWARPS;
     const int wb = min(nwords, warp * wpw), we = min(nwords, wb + wpw);
+    auto slab = [&](int b, uint32_t (&w)[CW]) {   // lane's words b + lane + 32 k
+#pragma unroll
+        for (int k = 0; k < CW; ++k) {
+            const int i = b + lane + 32 * k;
+            w[k] = i < we ? (i < full ? 0xffffffffu : __ldcg(maskw + i)) : 0u;
+        }
+    };
     int cnt = 0;
-    auto word = [&](int w) -> uint32_t { return w < full ? 0xffffffffu : __ldcg(maskw + w); };
-    for (int b = wb; b < we; b += 32) cnt += __popc(b + lane < we ? word(b + lane) : 0u);
+    for (int b = wb; b < we; b += 32 * CW) {
+        uint32_t w[CW];
+        slab(b, w);
+#pragma unroll
+        for (int k = 0; k < CW; ++k) cnt += __popc(w[k]);
+    }
     cnt = warp_sum_int(cnt);
     if (lane == 0) wsum[warp] = cnt;
     sync();
@@ -152,13 +164,17 @@ __device__ __forceinline__ void compact_words(const uint32_t *__restrict__ maskw
         total += wsum[w];
     }
     const uint32_t below = (1u << lane) - 1u;
-    for (int b = wb; b < we; b += 32) {
-        const uint32_t mine = b + lane < we ? word(b + lane) : 0u;
-        const int nk = min(32, we - b);
-        for (int k = 0; k < nk; ++k) {
-            const uint32_t m = __shfl_sync(0xffffffffu, mine, k);
-            if ((m >> lane) & 1u) idx[off + __popc(m & below)] = (b + k) * 32 + lane;
-            off += __popc(m);
+    for (int b = wb; b < we; b += 32 * CW) {
+        uint32_t w[CW];
+        slab(b, w);
+#pragma unroll
+        for (int k = 0; k < CW; ++k) {
+            const int nk = min(32, we - (b + 32 * k));
+            for (int q = 0; q < nk; ++q) {
+                const uint32_t m = __shfl_sync(0xffffffffu, w[k], q);
+                if ((m >> lane) & 1u) idx[off + __popc(m & below)] = (b + 32 * k + q) * 32 + lane;
+                off += __popc(m);
+            }
         }
     }
     if (threadIdx.x % (32 * NWARPS) == 0) *count = total;
