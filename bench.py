@@ -1,20 +1,22 @@
 """Benchmark: activation-sparse FFN decode tokens/s and achieved HBM GB/s on GB300.
 
-One step = one decode token through every layer of the stack (pi_decode_stack:
-predictor -> union mask -> gate/up gather -> W_down axpy -> deterministic reduce,
-per layer). Default workload: ReluLLaMA-7B-shaped stack (32 gated-ReLU FFN layers,
-d=4096, f=11008, bf16, predictor rank 1024), batch 1, synthetic seeded weights and
-inputs. Each step streams ~1.9 GB of distinct weights, far more than the 126 MB
-L2, so steps run with inputs larger than L2 (no flush needed).
+One step = one decode token (one per sequence of the batch) through every layer of
+the stack via pi_decode_stack: predictor -> union mask -> gate/up gather -> W_down
+axpy -> deterministic reduce, per layer. Default workload: ReluLLaMA-7B-shaped stack
+(32 gated-ReLU FFN layers, d=4096, f=11008, bf16, predictor rank 1024), batch 1,
+synthetic seeded weights and inputs. Each step streams ~1.9 GB of distinct weights,
+far more than the 129 MB L2, so steps run with inputs larger than L2 (no flush needed).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--batch B] [--no-cpu-baseline]
+                  [--workload NAME] [--batch B] [--layers L] [--rank R]
+                  [--hot-prefix-fraction F] [--hot-fraction G] [--no-cpu-baseline]
 
---impl reference times the CPU fp64 oracle (the reference arm of this build) on the
-host cores, on a bounded sample of the same workload. Under torchrun (N > 1) every
-rank decodes its own token stream with the same weights (independent sequences,
-weak scaling, no data-path collective); only a barrier and a max over ranks of the
-timed region are exchanged.
+--impl reference times the CPU fp64 oracle on the host cores, on a bounded sample
+of the same workload. --rank runs the predictor-rank sweep's variants, and
+--hot-prefix-fraction the hot-prefix variant of the method. Under torchrun (N > 1)
+every rank decodes its own token stream with the same weights (independent
+sequences, weak scaling, no data-path collective); only a barrier and a max over
+ranks of the timed region are exchanged.
 """
 from __future__ import annotations
 

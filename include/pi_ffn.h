@@ -45,7 +45,7 @@ extern "C" {
 typedef enum {
     PI_OK = 0,
     PI_ERR_INVALID_ARG = 1,   /* bad size, NULL / misaligned / host pointer, layer or batch out of range */
-    PI_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement (e.g. int4 with d % 128 != 0) */
+    PI_ERR_UNSUPPORTED = 2,   /* a valid request the library does not implement (e.g. int4 with d % 128 != 0) */
     PI_ERR_CUDA = 3,          /* a CUDA runtime call failed */
     PI_ERR_OOM = 4,           /* workspace allocation failed */
     PI_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up */
