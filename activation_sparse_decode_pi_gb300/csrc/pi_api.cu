@@ -132,6 +132,7 @@ struct pi_ffn {
     bool stack_ok = false;
     int n_hot = 0;                     // neurons [0, n_hot) expected to fire on most tokens
     int hot_prefix = 0;                // neurons [0, hot_prefix) computed on every token
+    int stack_p2 = 0;                  // owned P2 rows per CTA the persistent step stages in its ring
     StackLayer *stack_layers = nullptr;
     uint32_t *stack_mask = nullptr;
     float *stack_sumsq = nullptr;
@@ -596,6 +597,13 @@ void plan_stack(pi_ffn_t *h)
     h->off_ring = (int)off_ring;
     h->off_flags = (int)off_flags;
     h->off_mbar = (int)off_mbar;
+    // The ring is idle from the end of one layer's FFN to the next layer's logits: the next
+    // layer's owned P2 rows are copied into it then, as many as fit (PI_FFN_STACK_P2=0: none).
+    const char *p2env = std::getenv("PI_FFN_STACK_P2");
+    const size_t p2row = elt_row_bytes(D.pdtype, D.r);
+    h->stack_p2 = 0;
+    if (!(p2env && p2env[0] == '0') && p2row % 16 == 0)
+        h->stack_p2 = (int)std::min(own, (size_t)h->stack_ring / p2row);
     h->stack_ok = true;
 }
 
@@ -638,6 +646,7 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.hot_prefix = h->hot_prefix;
     a.hot_k = h->n_hot > 0 ? std::min((h->n_hot + h->nsm - 1) / h->nsm, h->stack_slots - 2) : 0;
     if (a.hot_k < 0) a.hot_k = 0;
+    a.p2_stage = a.hot_k > 0 ? 0 : h->stack_p2;   // the hot slots hold the ring between layers
     a.bias_bulk = D.f % 4 == 0 ? 1 : 0;
     for (const pi_layer_weights_t &w : h->layers)
         if (!w.b_gate) a.bias_bulk = 0;

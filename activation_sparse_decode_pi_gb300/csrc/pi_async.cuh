@@ -89,6 +89,13 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32
         : "memory");
 }
 
+// 4-byte global -> shared copy (cp.async); the issuing thread waits with cp_async_wait_all.
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Bring `bytes` (multiple of 16, 16-byte aligned) of global memory into L2 without waiting.
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
 {
@@ -131,9 +138,19 @@ __device__ __forceinline__ unsigned long long barrier_base(const unsigned long l
     return c - c % per_launch;
 }
 
-// Returns false in every thread of a CTA that gave up waiting (after recording PI_ERR_TIMEOUT).
+// Bulk copies a CTA may have in flight at a grid barrier: phase par[0] of *one (if >= 0) and
+// phase par[1] of each of many[0..nmany) (if >= 0). par lives in shared memory.
+struct PendingCopies {
+    uint64_t *one;
+    uint64_t *many;
+    int nmany;
+    const int *par;
+};
+
+// Returns false in every thread of a CTA that gave up waiting (after recording PI_ERR_TIMEOUT
+// and waiting, bounded, for the copies `pc` names to land).
 __device__ __forceinline__ bool grid_sync_to(unsigned long long *cnt, unsigned long long target, uint32_t *status,
-                                             int *s_flag)
+                                             int *s_flag, const PendingCopies *pc = nullptr)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -145,6 +162,9 @@ __device__ __forceinline__ bool grid_sync_to(unsigned long long *cnt, unsigned l
                 if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
                     set_status(status, ST_TIMEOUT);
                     ok = 0;
+                    if (pc && pc->par[0] >= 0) mbar_wait(pc->one, (uint32_t)pc->par[0]);
+                    if (pc && pc->par[1] >= 0)
+                        for (int k = 0; k < pc->nmany; ++k) mbar_wait(&pc->many[k], (uint32_t)pc->par[1]);
                     break;
                 }
                 __nanosleep(64);   // fewer polls on the counter's line while the arrivals land

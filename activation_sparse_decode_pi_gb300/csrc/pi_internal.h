@@ -54,6 +54,7 @@ struct StackArgs {
     int bias_bulk;                // gate biases ride in the row copies (every layer has one and f % 4 == 0)
     int hot_k;                    // ring slots per CTA held by hot owned neurons (loaded a layer ahead), <= slots - 2
     int hot_prefix;               // neurons below this are active without a logit
+    int p2_stage;                 // owned P2 rows per CTA copied into the ring ahead of their layer (0: none)
 };
 
 template <int WT>

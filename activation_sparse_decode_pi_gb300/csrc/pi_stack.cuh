@@ -124,6 +124,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     __shared__ float sbias[STACK_MAX_CHUNK];
     __shared__ float s_inv;
     __shared__ int s_flag;
+    __shared__ uint64_t s_p2bar;   // the staged P2 rows of the next layer have landed
+    __shared__ float spb[STACK_MAX_CHUNK];   // predictor bias of the owned rows, copied during phase A
+    __shared__ int s_pend[2];      // thread 0: parity of staged P2 copies not yet waited for, of the
+                                   // last hot-slot copies issued (-1: none)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x, c = blockIdx.x;
@@ -137,6 +141,12 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     const int K = c < f ? (f - 1 - c) / P + 1 : 0;          // owned neurons: i = c + P * k, k < K
     const int bias_off = ROWS * (rowb + sclb);               // 16-byte chunk holding the gate bias
     const bool bias_bulk = a.bias_bulk != 0;                 // the chunk stays inside b_gate only if f % 4 == 0
+    // Owned P2 rows k < KS of the next layer are copied into the ring once this layer's FFN is
+    // done with it (row k at ring + k * p2b); they land during the reduction and predictor
+    // phases, so the logits read them from shared memory. Rows below the hot prefix need none.
+    const int p2b = r * pb;
+    const int KS = min(K, a.p2_stage);
+    const int ks0 = a.hot_prefix > c ? min(KS, (a.hot_prefix - c + P - 1) / P) : 0;
     // Ring slots [0, HK) hold this CTA's hot owned neurons k < HK (loaded every layer before its
     // predictor runs: the copy for layer l is the slot's l-th, parity l & 1). Slots [HK, S) take
     // the other active neurons in list order: the cold neuron staged n-th in this launch goes to
@@ -145,7 +155,18 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     unsigned kb = 0;    // grid barriers passed in this launch
     auto sync_grid = [&]() -> bool {
         ++kb;
-        return grid_sync_to(a.bar, s_base + (unsigned long long)kb * a.nblocks, a.status, &s_flag);
+        const PendingCopies pc{&s_p2bar, mbar, min(a.hot_k, K), s_pend};
+        return grid_sync_to(a.bar, s_base + (unsigned long long)kb * a.nblocks, a.status, &s_flag, &pc);
+    };
+    auto expect_p2 = [&]() {
+        if (tid == 0) mbar_arrive_expect_tx(&s_p2bar, (uint32_t)((KS - ks0) * p2b));
+    };
+    auto stage_p2 = [&](const StackLayer &L) {   // one copy per thread; the ring is free and expect_p2 ran
+        if (tid >= ks0 && tid < KS) {
+            fence_proxy_async_smem();
+            bulk_g2s(ring + (size_t)tid * p2b, (const char *)L.p2 + (size_t)(c + (size_t)P * tid) * p2b, (uint32_t)p2b,
+                     &s_p2bar);
+        }
     };
 
     // this CTA's P1 rows, one chunk per lane and row at a time
@@ -153,9 +174,9 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     const int pa_per = (nchp + SNW - 1) / SNW, pa_cb = warp * pa_per, pa_ce = min(nchp, pa_cb + pa_per);
     RowChunks<PT, 8, 1> pa;
     // the rest of this CTA's predictor slice, into L2
-    // (one prefetch per thread: thread k < K takes owned P2 row k, the last thread the P1 rows)
+    // (one prefetch per thread: thread k in [KS, K) takes owned P2 row k, the last thread the P1 rows)
     auto prefetch_predictor = [&](const StackLayer &L) {
-        if (tid < K) prefetch_l2((const char *)L.p2 + (size_t)(c + (size_t)P * tid) * r * pb, r * pb);
+        if (tid >= KS && tid < K) prefetch_l2((const char *)L.p2 + (size_t)(c + (size_t)P * tid) * r * pb, r * pb);
         if (tid == STACK_NT - 1) prefetch_l2_range((const char *)L.p1 + (size_t)k0 * d * pb, (size_t)(k1 - k0) * d * pb);
     };
 
@@ -177,12 +198,17 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     // ---------------------------------------------------------------- phase 0
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&mbar[s], 1);
+        mbar_init(&s_p2bar, 1);
         fence_mbar_init();
+        s_pend[0] = KS > 0 ? 0 : -1;
+        s_pend[1] = a.hot_k > 0 ? 0 : -1;
         s_base = barrier_base(a.bar, (unsigned long long)(3 * a.L) * a.nblocks);
     }
+    if (KS > 0) expect_p2();
     prefetch_predictor(a.layers[0]);
     __syncthreads();
     issue_hot(a.layers[0], -1);
+    if (KS > 0) stage_p2(a.layers[0]);
     if (a.idx_out)
         for (int i = c * STACK_NT + tid; i < a.L * W; i += P * STACK_NT) a.maskw[i] = 0u;
     if (a.counts && c == 0)
@@ -214,6 +240,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
         {
             constexpr int QP = VP / 4;
             load_p1_chunk<PT>(pa, Lw.p1, k0, k1, nchp, pa_cb + lane, pa_ce);   // requested before u is staged
+            if (tid < K) {   // the logits' biases, waited for before this phase's grid barrier
+                if (Lw.bp) cp_async4(&spb[tid], Lw.bp + c + P * tid);
+                else spb[tid] = 0.f;
+            }
             for (int t = tid; t < d / 4; t += STACK_NT) {
                 float4 v = __ldcg(reinterpret_cast<const float4 *>(xl) + t);
                 v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
@@ -248,6 +278,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 for (int w = 0; w < SNW; ++w) v += red[0][w][tid];   // fixed order
                 a.hp[k0 + tid] = fmaxf(v, 0.f);
             }
+            cp_async_wait_all();
         }
         if (!sync_grid()) return;
 
@@ -256,8 +287,26 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             // logits of the owned rows: warp w takes rows k = w, w + 16, ..., five at a time
             const int nchr = r / VP;
             const uint4 *row[5];
-            const __half *srow[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
             RowChunks<PT, 5, 4> rc;
+            // rows kbase + SNW * q: a staged row is read from the ring (the generic loads below
+            // take either space), the others from memory
+            auto rows_at = [&](int kbase) {
+                owned_rows<5>(row, Lw.p2, kbase, SNW, K, c, P, nchr, a.hot_prefix);
+#pragma unroll
+                for (int q = 0; q < 5; ++q) {
+                    const int k = kbase + SNW * q;
+                    if (k < KS && row[q]) row[q] = reinterpret_cast<const uint4 *>(ring) + (size_t)k * nchr;
+                }
+            };
+            auto issue_rows = [&](int cc) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int ci = cc + 32 * i;
+#pragma unroll
+                    for (int q = 0; q < 5; ++q)
+                        rc.w[q][i] = ci < nchr && row[q] != nullptr ? row[q][ci] : make_uint4(0u, 0u, 0u, 0u);
+                }
+            };
             // hp is requested first, so its reads (L2 hits) do not queue behind the P2 rows
             const int r4 = r / 4;
             float4 hv[2];
@@ -266,32 +315,40 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 const int t = tid + u * STACK_NT;
                 hv[u] = t < r4 ? __ldcg(reinterpret_cast<const float4 *>(a.hp) + t) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            owned_rows<5>(row, Lw.p2, warp, SNW, K, c, P, nchr, a.hot_prefix);
-            rows_issue(rc, row, srow, lane, nchr);                  // before hp is staged
+            const bool p2ok = KS == 0 || mbar_wait(&s_p2bar, (uint32_t)l & 1u);
+            rows_at(warp);
+            issue_rows(lane);                                        // before hp is staged
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 constexpr int QH = VP / 4;
                 const int t = tid + u * STACK_NT;
                 if (t < r4) hp4[(t % QH) * nchr + t / QH] = hv[u];   // planar layout of the row dot products
             }
-            __syncthreads();
+            if (!__syncthreads_and(p2ok)) {
+                if (tid == 0) {
+                    set_status(a.status, ST_TIMEOUT);
+                    mbar_wait(&s_p2bar, (uint32_t)l & 1u);
+                }
+                return;
+            }
+            if (tid == 0) s_pend[0] = -1;
             for (int kbase = warp; kbase < K; kbase += SNW * 5) {
                 if (kbase != warp) {
-                    owned_rows<5>(row, Lw.p2, kbase, SNW, K, c, P, nchr, a.hot_prefix);
-                    rows_issue(rc, row, srow, lane, nchr);
+                    rows_at(kbase);
+                    issue_rows(lane);
                 }
                 float acc[5][1] = {{0.f}, {0.f}, {0.f}, {0.f}, {0.f}};
                 for (int cc = lane;;) {
                     rows_consume<PT, 5, 4, 1>(rc, cc, nchr, hp4, r, acc);
                     cc += 32 * 4;
                     if (cc >= nchr) break;
-                    rows_issue(rc, row, srow, cc, nchr);
+                    issue_rows(cc);
                 }
 #pragma unroll
                 for (int q = 0; q < 5; ++q) {
                     const int k = kbase + SNW * q;
                     const int i = c + P * k;
-                    const float z = warp_sum(acc[q][0]) + ((k < K && Lw.bp) ? __ldg(Lw.bp + i) : 0.f);
+                    const float z = warp_sum(acc[q][0]) + (k < K ? spb[k] : 0.f);
                     if (lane == 0 && k < K) sflag[k] = (i < a.hot_prefix || z > a.tau) ? 1 : 0;
                 }
             }
@@ -504,6 +561,14 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             if (l + 1 < a.L && a.hot_k > 0) {
                 __syncthreads();
                 issue_hot(a.layers[l + 1], l);
+                if (tid == 0) s_pend[1] = (l + 1) & 1;
+            }
+            // likewise the next layer's staged P2 rows
+            if (l + 1 < a.L && KS > 0) {
+                expect_p2();
+                __syncthreads();
+                stage_p2(a.layers[l + 1]);
+                if (tid == 0) s_pend[0] = (l + 1) & 1;
             }
         }
         if (!sync_grid()) return;

@@ -114,7 +114,6 @@ __device__ __forceinline__ void cp_async_wait()
 {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Arrive on `bar` once every cp.async this thread issued so far has completed (the barrier's
 // expected count includes this arrival).

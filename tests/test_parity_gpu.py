@@ -365,6 +365,57 @@ def test_decode_stack_hot_neurons_bit_identical(P, wi):
     ffn.close()
 
 
+def _with_env(name, value, fn):
+    import os
+
+    old = os.environ.get(name)
+    os.environ[name] = value
+    try:
+        return fn()
+    finally:
+        if old is None:
+            del os.environ[name]
+        else:
+            os.environ[name] = old
+
+
+# d 1024 with f 30000 and r 1024: ~198 owned P2 rows of 2 KB per CTA, more than the ring holds
+P2_WIDE_SHAPE = dict(d=1024, f=30000, r=1024)
+
+
+@pytest.mark.parametrize("wi,shape", [(wi, STACK_SHAPE) for wi in range(5)] + [(1, P2_WIDE_SHAPE), (3, P2_WIDE_SHAPE)])
+def test_decode_stack_p2_staging_bit_identical(P, wi, shape):
+    """Copying the next layer's owned P2 rows into shared memory ahead of their logits (all of
+    them, or the first ones when they do not all fit) changes nothing in the output bits."""
+    w = _wl(wi, shape, n_layers=3)
+    layers = build_layers(w, range(w.n_layers))
+    X = make_inputs(w, 2, 1, seed=13, device="cpu").numpy()
+    staged = _handle(P, w, [g for g, _ in layers], stack_kernel=True)
+    plain = _with_env("PI_FFN_STACK_P2", "0", lambda: _handle(P, w, [g for g, _ in layers], stack_kernel=True))
+    for H in (0, 700):
+        for ffn in (staged, plain):
+            ffn.set_hot_prefix(H)
+        for t in range(X.shape[0]):
+            outs = []
+            for ffn in (staged, plain):
+                counts = torch.zeros(w.n_layers, dtype=torch.int32, device="cuda")
+                idx_out = torch.zeros((w.n_layers, w.f), dtype=torch.int32, device="cuda")
+                P.pi_profile_begin(ffn.h)
+                xo = ffn.decode_stack(to_dev(X[t]), counts=counts, idx_out=idx_out)
+                prof = P.pi_profile_end(ffn.h)
+                assert prof["decode_stack"][1] == 1, prof
+                outs.append((xo.clone(), counts.clone(), idx_out.clone()))
+            assert torch.equal(outs[0][0], outs[1][0]), (H, t)
+            assert torch.equal(outs[0][1], outs[1][1]) and torch.equal(outs[0][2], outs[1][2]), (H, t)
+            if H:
+                cg, ig = outs[0][1].cpu().numpy(), outs[0][2].cpu().numpy()
+                for l in range(w.n_layers):
+                    assert np.array_equal(ig[l, :H], np.arange(H)), l
+    for ffn in (staged, plain):
+        assert ffn.status() == 0
+        ffn.close()
+
+
 # ------------------------------------------------------------------ hot-prefix variant --------
 
 def _check_list(gi, pr, H):
