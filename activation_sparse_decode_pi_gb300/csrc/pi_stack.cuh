@@ -41,6 +41,7 @@
 namespace pi {
 
 constexpr int SNW = STACK_NT / 32;
+static_assert(SNW == 16, "the batch reduction maps the 16 warps onto half a warp's lanes");
 
 template <int WT>
 __host__ __device__ constexpr int weight_row_bytes(int d)
@@ -75,6 +76,33 @@ __device__ __forceinline__ void owned_rows(const uint4 *(&row)[RW], const void *
         const int i = c + P * k;
         row[q] = (k < K && i >= hot) ? reinterpret_cast<const uint4 *>(m) + (size_t)i * nch : nullptr;
     }
+}
+
+// Sum of each of N (4 or 8) per-lane values over the warp, transposed: lane L ends with the sum
+// of value L / (32 / N). The value count halves at each of the first log2(N) butterfly levels
+// (lanes with the level's bit set keep the upper half), so the N sums take N - 1 + 5 - log2(N)
+// shuffles instead of 5 N; the order of the additions is fixed.
+template <int N>
+__device__ __forceinline__ float warp_transpose_sum(const float (&v)[N], int lane)
+{
+    static_assert(N == 4 || N == 8, "value count");
+    float w[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) w[j] = v[j];
+    int off = 16;
+#pragma unroll
+    for (int h = N / 2; h >= 1; h /= 2, off /= 2) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int j = 0; j < h; ++j) {
+            const float send = up ? w[j] : w[j + h];
+            const float keep = up ? w[j + h] : w[j];
+            w[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+#pragma unroll
+    for (; off >= 1; off /= 2) w[0] += __shfl_xor_sync(0xffffffffu, w[0], off);
+    return w[0];
 }
 
 // Bulk-copy neuron i's rows of layer Lw (gate(, up), W_down; int4 scales; the 16-byte chunk
@@ -425,27 +453,45 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 #pragma unroll
                 for (int e = 0; e < VW; ++e) yr[cc][e] = 0.f;
 
-            // neurons are reduced a batch at a time, in list order (hot ones first): one CTA-wide
+            // Neurons are reduced a batch at a time, in list order (hot ones first): one CTA-wide
             // synchronisation per batch. Hot batches take up to NB resident neurons; a cold batch
             // waits only on copies issued at least one batch earlier, which needs 2 * nbc <= SC.
+            // Cold list entry m0 + k sits in slot HK + cs + k (wrapping at SC, parity flipped on the
+            // wrap), where (cs, cp) are the slot and parity of the batch's first entry.
             constexpr int NB = 4;
+            constexpr int NV = KIND == KIND_GATED ? 2 * NB : NB;   // per-warp partial sums of a batch
             const int nbc = max(1, min(NB, SC / 2));
+            uint32_t cs = cseq % (uint32_t)SC, cp = (cseq / (uint32_t)SC) & 1u;
+            auto slot_at = [&](int m0, bool cold, int k, uint32_t &par) -> int {
+                if (!cold) {
+                    par = (uint32_t)l & 1u;
+                    return (sneur[m0 + k] - c) / P;
+                }
+                uint32_t sk = cs + (uint32_t)k;
+                par = cp;
+                if (sk >= (uint32_t)SC) {
+                    sk -= (uint32_t)SC;
+                    par ^= 1u;
+                }
+                return HK + (int)sk;
+            };
             int bi = 0;
             for (int m0 = 0; m0 < nn; ++bi) {
                 const bool cold = m0 >= nh;
                 const int mb = cold ? min(nbc, nn - m0) : min(NB, nh - m0);
                 bool got = true;
-                float pg[NB], pu[NB];
+                float v[NV];   // gated: gate and up partial of neuron k at 2k, 2k + 1; else gate at k
+#pragma unroll
+                for (int j = 0; j < NV; ++j) v[j] = 0.f;
 #pragma unroll
                 for (int k = 0; k < NB; ++k) {
-                    pg[k] = 0.f;
-                    pu[k] = 0.f;
-                    if (k >= mb) continue;
+                    if (k >= mb) break;
                     uint32_t par;
-                    const int slot = slot_of(m0 + k, par);
+                    const int slot = slot_at(m0, cold, k, par);
                     const unsigned char *sl = ring + (size_t)slot * a.slot_bytes;
                     got = got && mbar_wait(&mbar[slot], par);
                     if (!got) continue;
+                    constexpr int GI = KIND == KIND_GATED ? 2 : 1;
 #pragma unroll
                     for (int cc = 0; cc < CPT; ++cc) {
                         const int ci = tid + cc * STACK_NT;
@@ -457,36 +503,31 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                             float tg = 0.f;
 #pragma unroll
                             for (int e = 0; e < 32; ++e) tg = fmaf(nib(ag[e >> 3], e & 7), ur[cc][e], tg);
-                            pg[k] = fmaf(__half2float(ss[ci >> 2]), tg, pg[k]);
+                            v[GI * k] = fmaf(__half2float(ss[ci >> 2]), tg, v[GI * k]);
                             if (KIND == KIND_GATED) {
                                 const uint4 wu = reinterpret_cast<const uint4 *>(sl + rowb)[ci];
                                 const uint32_t au[4] = {wu.x, wu.y, wu.z, wu.w};
                                 float tu = 0.f;
 #pragma unroll
                                 for (int e = 0; e < 32; ++e) tu = fmaf(nib(au[e >> 3], e & 7), ur[cc][e], tu);
-                                pu[k] = fmaf(__half2float(ss[d / 128 + (ci >> 2)]), tu, pu[k]);
+                                v[GI * k + 1] = fmaf(__half2float(ss[d / 128 + (ci >> 2)]), tu, v[GI * k + 1]);
                             }
                         } else {
                             float wf[VW];
                             unpack<WT>(wg, wf);
 #pragma unroll
-                            for (int e = 0; e < VW; ++e) pg[k] = fmaf(wf[e], ur[cc][e], pg[k]);
+                            for (int e = 0; e < VW; ++e) v[GI * k] = fmaf(wf[e], ur[cc][e], v[GI * k]);
                             if (KIND == KIND_GATED) {
                                 unpack<WT>(reinterpret_cast<const uint4 *>(sl + rowb)[ci], wf);
 #pragma unroll
-                                for (int e = 0; e < VW; ++e) pu[k] = fmaf(wf[e], ur[cc][e], pu[k]);
+                                for (int e = 0; e < VW; ++e) v[GI * k + 1] = fmaf(wf[e], ur[cc][e], v[GI * k + 1]);
                             }
                         }
                     }
                 }
-#pragma unroll
-                for (int k = 0; k < NB; ++k) {
-                    pg[k] = warp_sum(pg[k]);
-                    if (KIND == KIND_GATED) pu[k] = warp_sum(pu[k]);
-                    if (lane == 0) {
-                        red[bi & 1][warp][2 * k] = pg[k];
-                        red[bi & 1][warp][2 * k + 1] = pu[k];
-                    }
+                {   // lane L ends with this warp's sum of value L / (32 / NV)
+                    const float t = warp_transpose_sum<NV>(v, lane);
+                    if ((lane & (32 / NV - 1)) == 0) red[bi & 1][warp][lane / (32 / NV)] = t;
                 }
                 if (!__syncthreads_and(got)) {
                     // give up: wait (bounded) for this CTA's copies still in flight, then leave
@@ -501,28 +542,31 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     }
                     return;
                 }
-                // the previous cold batch's slots are free: refill them
+                // the previous cold batch's slots are free: entry k + SC takes entry k's slot
                 if (cold && m0 - nbc >= nh && lane == 0 && warp < nbc) {
                     const int k = m0 - nbc + warp;
                     if (k + SC < nn) {
                         fence_proxy_async_smem();
-                        uint32_t par;
-                        stage_neuron<WT, KIND>(a, Lw, ring, mbar, slot_of(k + SC, par), sneur[k + SC]);
+                        int sk = (int)cs - nbc + warp;
+                        if (sk < 0) sk += SC;
+                        stage_neuron<WT, KIND>(a, Lw, ring, mbar, HK + sk, sneur[k + SC]);
                     }
                 }
 #pragma unroll
                 for (int k = 0; k < NB; ++k) {
                     if (k >= mb) break;
                     uint32_t par;
-                    const unsigned char *sl = ring + (size_t)slot_of(m0 + k, par) * a.slot_bytes;
-                    float g = 0.f, up = 0.f;
-                    for (int w = 0; w < SNW; ++w) {   // fixed order
-                        g += red[bi & 1][w][2 * k];
-                        up += red[bi & 1][w][2 * k + 1];
-                    }
+                    const unsigned char *sl = ring + (size_t)slot_at(m0, cold, k, par) * a.slot_bytes;
+                    // neuron k's partial sums of the 16 warps, added in a fixed butterfly order
+                    float sg = KIND == KIND_GATED ? red[bi & 1][lane & 15][2 * k + (lane >> 4)] : red[bi & 1][lane & 15][k];
+                    sg += __shfl_xor_sync(0xffffffffu, sg, 8);
+                    sg += __shfl_xor_sync(0xffffffffu, sg, 4);
+                    sg += __shfl_xor_sync(0xffffffffu, sg, 2);
+                    sg += __shfl_xor_sync(0xffffffffu, sg, 1);
+                    float g = __shfl_sync(0xffffffffu, sg, 0);
                     g += bias_bulk ? reinterpret_cast<const float *>(sl + bias_off)[sneur[m0 + k] & 3] : sbias[m0 + k];
                     float hv = fmaxf(g, 0.f);
-                    if (KIND == KIND_GATED) hv *= up;
+                    if (KIND == KIND_GATED) hv *= __shfl_sync(0xffffffffu, sg, 16);
                     const uint4 *wd = reinterpret_cast<const uint4 *>(sl + (ROWS - 1) * rowb);
 #pragma unroll
                     for (int cc = 0; cc < CPT; ++cc) {
@@ -541,6 +585,13 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 #pragma unroll
                             for (int e = 0; e < VW; ++e) yr[cc][e] = fmaf(hv, wf[e], yr[cc][e]);
                         }
+                    }
+                }
+                if (cold) {
+                    cs += (uint32_t)mb;
+                    if (cs >= (uint32_t)SC) {
+                        cs -= (uint32_t)SC;
+                        cp ^= 1u;
                     }
                 }
                 m0 += mb;
