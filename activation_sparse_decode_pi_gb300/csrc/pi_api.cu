@@ -603,7 +603,7 @@ void plan_stack(pi_ffn_t *h)
     const size_t p2row = elt_row_bytes(D.pdtype, D.r);
     h->stack_p2 = 0;
     if (!(p2env && p2env[0] == '0') && p2row % 16 == 0)
-        h->stack_p2 = (int)std::min(own, (size_t)h->stack_ring / p2row);
+        h->stack_p2 = (int)std::min(own, (size_t)h->stack_ring / (size_t)stack_p2_stride((int)p2row));
     h->stack_ok = true;
 }
 

@@ -33,6 +33,14 @@ struct StackLayer {
     const float *bp;              // predictor bias or NULL
 };
 
+// Byte stride of the P2 rows the persistent step stages in shared memory: the row plus 16 or
+// 32 bytes, so that the stride is an odd number of 16-byte units and eight consecutive rows
+// start in eight different bank groups.
+__host__ __device__ inline int stack_p2_stride(int row_bytes)
+{
+    return row_bytes + ((row_bytes >> 4) & 1 ? 32 : 16);
+}
+
 struct StackArgs {
     const StackLayer *layers;     // device array [L]
     int L, d, f, r;

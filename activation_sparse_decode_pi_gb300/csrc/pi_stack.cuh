@@ -37,6 +37,7 @@
 #include "pi_common.cuh"
 #include "pi_internal.h"
 #include "pi_rowdot.cuh"
+#include "pi_umma.cuh"
 
 namespace pi {
 
@@ -105,6 +106,32 @@ __device__ __forceinline__ float warp_transpose_sum(const float (&v)[N], int lan
     return w[0];
 }
 
+// Four 8 x 8 tiles of 16-bit elements from shared memory (lane l gives the address of row
+// l % 8 of tile l / 8), one 32-bit register per tile and lane.
+__device__ __forceinline__ void ldsm_x4(uint32_t saddr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr));
+}
+
+// D[16 x 8] += A[16 x 16] * B[16 x 8], 16-bit operands of type PT, fp32 accumulators
+// (warp-level mma.sync; fragments in the m16n8k16 layouts).
+template <int PT>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    if constexpr (PT == DT_BF16)
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                     "{%8, %9}, {%0, %1, %2, %3};"
+                     : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                     "{%8, %9}, {%0, %1, %2, %3};"
+                     : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Bulk-copy neuron i's rows of layer Lw (gate(, up), W_down; int4 scales; the 16-byte chunk
 // holding its gate bias) into ring slot `slot`; completion is counted on the slot's mbarrier.
 // Everything is derived from the launch arguments, so callers keep no state for it.
@@ -170,9 +197,9 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     const int bias_off = ROWS * (rowb + sclb);               // 16-byte chunk holding the gate bias
     const bool bias_bulk = a.bias_bulk != 0;                 // the chunk stays inside b_gate only if f % 4 == 0
     // Owned P2 rows k < KS of the next layer are copied into the ring once this layer's FFN is
-    // done with it (row k at ring + k * p2b); they land during the reduction and predictor
+    // done with it (row k at ring + k * p2st); they land during the reduction and predictor
     // phases, so the logits read them from shared memory. Rows below the hot prefix need none.
-    const int p2b = r * pb;
+    const int p2b = r * pb, p2st = stack_p2_stride(p2b);
     const int KS = min(K, a.p2_stage);
     const int ks0 = a.hot_prefix > c ? min(KS, (a.hot_prefix - c + P - 1) / P) : 0;
     // Ring slots [0, HK) hold this CTA's hot owned neurons k < HK (loaded every layer before its
@@ -192,7 +219,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     auto stage_p2 = [&](const StackLayer &L) {   // one copy per thread; the ring is free and expect_p2 ran
         if (tid >= ks0 && tid < KS) {
             fence_proxy_async_smem();
-            bulk_g2s(ring + (size_t)tid * p2b, (const char *)L.p2 + (size_t)(c + (size_t)P * tid) * p2b, (uint32_t)p2b,
+            bulk_g2s(ring + (size_t)tid * p2st, (const char *)L.p2 + (size_t)(c + (size_t)P * tid) * p2b, (uint32_t)p2b,
                      &s_p2bar);
         }
     };
@@ -323,7 +350,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 #pragma unroll
                 for (int q = 0; q < 5; ++q) {
                     const int k = kbase + SNW * q;
-                    if (k < KS && row[q]) row[q] = reinterpret_cast<const uint4 *>(ring) + (size_t)k * nchr;
+                    if (k < KS && row[q]) row[q] = reinterpret_cast<const uint4 *>(ring + (size_t)k * p2st);
                 }
             };
             auto issue_rows = [&](int cc) {
@@ -344,40 +371,101 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 hv[u] = t < r4 ? __ldcg(reinterpret_cast<const float4 *>(a.hp) + t) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             const bool p2ok = KS == 0 || mbar_wait(&s_p2bar, (uint32_t)l & 1u);
-            rows_at(warp);
-            issue_rows(lane);                                        // before hp is staged
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                constexpr int QH = VP / 4;
-                const int t = tid + u * STACK_NT;
-                if (t < r4) hp4[(t % QH) * nchr + t / QH] = hv[u];   // planar layout of the row dot products
-            }
-            if (!__syncthreads_and(p2ok)) {
+            // joint decision: every thread saw the staged rows land, or the CTA leaves
+            auto staged_ok = [&]() -> bool {
+                if (__syncthreads_and(p2ok)) {
+                    if (tid == 0) s_pend[0] = -1;
+                    return true;
+                }
                 if (tid == 0) {
                     set_status(a.status, ST_TIMEOUT);
                     mbar_wait(&s_p2bar, (uint32_t)l & 1u);
                 }
-                return;
-            }
-            if (tid == 0) s_pend[0] = -1;
-            for (int kbase = warp; kbase < K; kbase += SNW * 5) {
-                if (kbase != warp) {
-                    rows_at(kbase);
-                    issue_rows(lane);
-                }
-                float acc[5][1] = {{0.f}, {0.f}, {0.f}, {0.f}, {0.f}};
-                for (int cc = lane;;) {
-                    rows_consume<PT, 5, 4, 1>(rc, cc, nchr, hp4, r, acc);
-                    cc += 32 * 4;
-                    if (cc >= nchr) break;
-                    issue_rows(cc);
-                }
+                return false;
+            };
+            // Every owned row staged and 16-bit: the logits are one small contraction on the tensor
+            // cores, [16-row tile of P2 rows] x [hp_hi hp_lo 0 ... 0] per mma.sync, hp entering as
+            // hi + lo halves in the predictor's type (so ~16 bits of it, with fp32 accumulation).
+            bool tcl = false;
+            if constexpr (PT == DT_BF16 || PT == DT_F16) tcl = KS == K && K > 0 && (r & 15) == 0;
+            if (tcl) {
+                uint32_t *bfr = reinterpret_cast<uint32_t *>(hp4);   // B fragments [r/16][8 lanes][2]
 #pragma unroll
-                for (int q = 0; q < 5; ++q) {
-                    const int k = kbase + SNW * q;
-                    const int i = c + P * k;
-                    const float z = warp_sum(acc[q][0]) + (k < K ? spb[k] : 0.f);
-                    if (lane == 0 && k < K) sflag[k] = (i < a.hot_prefix || z > a.tau) ? 1 : 0;
+                for (int u = 0; u < 2; ++u) {
+                    const int t = tid + u * STACK_NT;
+                    if (t >= r4) continue;
+                    const float e[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {   // element pair p = 2t + h: k = 2p, 2p + 1
+                        uint16_t h0, l0, h1, l1;
+                        split16<PT>(e[2 * h], h0, l0);
+                        split16<PT>(e[2 * h + 1], h1, l1);
+                        const int p = 2 * t + h, s16 = p >> 3, w = p & 7;
+                        const int ln = w & 3, reg = w >> 2;   // lane (column 0 = hi) and register of the pair
+                        bfr[(s16 * 8 + ln) * 2 + reg] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+                        bfr[(s16 * 8 + ln + 4) * 2 + reg] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+                    }
+                }
+                if (!staged_ok()) return;
+                // units (tile t, k part g): G warps share a tile when there are fewer tiles than warps
+                float *zp = reinterpret_cast<float *>(scr4);
+                const int MT = (K + 15) >> 4, NKS = r >> 4;
+                const int G = MT >= SNW ? 1 : SNW / MT;
+                for (int u = warp; u < MT * G; u += SNW) {
+                    const int t = u / G, g = u - t * G;
+                    const int s0 = g * NKS / G, s1 = (g + 1) * NKS / G;
+                    const int rw = min(t * 16 + (lane & 15), K - 1);   // rows past K repeat row K - 1
+                    const uint32_t ab = smem_u32(ring) + (uint32_t)(rw * p2st) + (uint32_t)(lane >> 4) * 16u;
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int s16 = s0; s16 < s1; ++s16) {
+                        uint32_t af[4];
+                        ldsm_x4(ab + (uint32_t)s16 * 32u, af);
+                        const uint2 bf =
+                            lane < 8 ? reinterpret_cast<const uint2 *>(bfr)[s16 * 8 + lane] : make_uint2(0u, 0u);
+                        mma_16816<PT>(acc, af, bf.x, bf.y);
+                    }
+                    if ((lane & 3) == 0) {   // columns 0 (hi part) and 1 (lo part) of rows lane/4, lane/4 + 8
+                        zp[u * 16 + (lane >> 2)] = acc[0] + acc[1];
+                        zp[u * 16 + (lane >> 2) + 8] = acc[2] + acc[3];
+                    }
+                }
+                __syncthreads();
+                for (int k = tid; k < K; k += STACK_NT) {
+                    const int t = k >> 4;
+                    float z = 0.f;
+                    for (int g = 0; g < G; ++g) z += zp[(t * G + g) * 16 + (k & 15)];   // fixed order
+                    z += spb[k];
+                    sflag[k] = (c + P * k < a.hot_prefix || z > a.tau) ? 1 : 0;
+                }
+            } else {
+                rows_at(warp);
+                issue_rows(lane);                                    // before hp is staged
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    constexpr int QH = VP / 4;
+                    const int t = tid + u * STACK_NT;
+                    if (t < r4) hp4[(t % QH) * nchr + t / QH] = hv[u];   // planar layout of the row dot products
+                }
+                if (!staged_ok()) return;
+                for (int kbase = warp; kbase < K; kbase += SNW * 5) {
+                    if (kbase != warp) {
+                        rows_at(kbase);
+                        issue_rows(lane);
+                    }
+                    float acc[5][1] = {{0.f}, {0.f}, {0.f}, {0.f}, {0.f}};
+                    for (int cc = lane;;) {
+                        rows_consume<PT, 5, 4, 1>(rc, cc, nchr, hp4, r, acc);
+                        cc += 32 * 4;
+                        if (cc >= nchr) break;
+                        issue_rows(cc);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 5; ++q) {
+                        const int k = kbase + SNW * q;
+                        const int i = c + P * k;
+                        const float z = warp_sum(acc[q][0]) + (k < K ? spb[k] : 0.f);
+                        if (lane == 0 && k < K) sflag[k] = (i < a.hot_prefix || z > a.tau) ? 1 : 0;
+                    }
                 }
             }
             __syncthreads();

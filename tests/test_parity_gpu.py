@@ -274,43 +274,70 @@ def _handle(P, w, layers, stack_kernel: bool):
             os.environ["PI_FFN_STACK_KERNEL"] = old
 
 
+# r % 16 == 0 with 16-bit predictor weights: a CTA whose owned P2 rows are all staged in
+# shared memory computes its logits on the tensor cores (mma.sync); r = 136 keeps them on
+# the CUDA cores
+STACK_SHAPE_TC = dict(d=2048, f=3001, r=144)
+
+
+def _stack_vs_oracle(P, w, layers, X, ffn, tag):
+    """One persistent or multi-kernel decode step per token of X against the oracle: the
+    active lists agree outside the band, and the output within the dtype's tolerance."""
+    for t in range(X.shape[0]):
+        counts = torch.zeros(w.n_layers, dtype=torch.int32, device="cuda")
+        idx_out = torch.zeros((w.n_layers, w.f), dtype=torch.int32, device="cuda")
+        xo = ffn.decode_stack(to_dev(X[t]), counts=counts, idx_out=idx_out)
+        xo2 = ffn.decode_stack(to_dev(X[t]), counts=counts, idx_out=idx_out).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(xo, xo2), "decode step is not deterministic"
+        st = oracle.stack(X[t].astype(np.float64), [o for _, o in layers], w.kind, w.wdtype, w.pdtype)
+        cg, ig = counts.cpu().numpy(), idx_out.cpu().numpy()
+        same = True
+        for l in range(w.n_layers):
+            gi = ig[l, : cg[l]]
+            assert np.all(np.diff(gi) > 0)
+            diff = np.setxor1d(gi, st["idx"][l])
+            if diff.size:
+                assert np.all(st["zmin"][l][diff] < oracle.BAND), (tag, l, diff)
+                same = False
+                break
+        if same:
+            err = rel_l2(xo.cpu().numpy() - X[t], st["x_out"] - X[t])
+            assert err <= TOL[w.wdtype], (tag, err)
+
+
+@pytest.mark.parametrize("shape", [STACK_SHAPE, STACK_SHAPE_TC], ids=["r136", "r144"])
 @pytest.mark.parametrize("wi", range(5))
-def test_decode_stack_both_paths_batch1(P, wi):
+def test_decode_stack_both_paths_batch1(P, wi, shape):
     """Batch 1: the single persistent kernel and the multi-kernel step both match the oracle."""
-    w = _wl(wi, STACK_SHAPE, n_layers=3)
+    w = _wl(wi, shape, n_layers=3)
     layers = build_layers(w, range(w.n_layers))
     X = make_inputs(w, 2, 1, seed=5, device="cpu").numpy()
     for stack_kernel in (True, False):
         ffn = _handle(P, w, [g for g, _ in layers], stack_kernel)
-        for t in range(X.shape[0]):
-            counts = torch.zeros(w.n_layers, dtype=torch.int32, device="cuda")
-            idx_out = torch.zeros((w.n_layers, w.f), dtype=torch.int32, device="cuda")
-            P.pi_profile_begin(ffn.h)
-            xo = ffn.decode_stack(to_dev(X[t]), counts=counts, idx_out=idx_out)
-            prof = P.pi_profile_end(ffn.h)
-            if stack_kernel:
-                assert prof["decode_stack"][1] == 1 and prof["ffn_h"][1] == 0, prof
-            else:
-                assert prof["decode_stack"][1] == 0 and prof["ffn_h"][1] == w.n_layers, prof
-            xo2 = ffn.decode_stack(to_dev(X[t]), counts=counts, idx_out=idx_out).clone()
-            torch.cuda.synchronize()
-            assert torch.equal(xo, xo2), "decode step is not deterministic"
-            st = oracle.stack(X[t].astype(np.float64), [o for _, o in layers], w.kind, w.wdtype, w.pdtype)
-            cg, ig = counts.cpu().numpy(), idx_out.cpu().numpy()
-            same = True
-            for l in range(w.n_layers):
-                gi = ig[l, : cg[l]]
-                assert np.all(np.diff(gi) > 0)
-                diff = np.setxor1d(gi, st["idx"][l])
-                if diff.size:
-                    assert np.all(st["zmin"][l][diff] < oracle.BAND), (stack_kernel, l, diff)
-                    same = False
-                    break
-            if same:
-                err = rel_l2(xo.cpu().numpy() - X[t], st["x_out"] - X[t])
-                assert err <= TOL[w.wdtype], (stack_kernel, err)
+        P.pi_profile_begin(ffn.h)
+        ffn.decode_stack(to_dev(X[0]))
+        prof = P.pi_profile_end(ffn.h)
+        if stack_kernel:
+            assert prof["decode_stack"][1] == 1 and prof["ffn_h"][1] == 0, prof
+        else:
+            assert prof["decode_stack"][1] == 0 and prof["ffn_h"][1] == w.n_layers, prof
+        _stack_vs_oracle(P, w, layers, X, ffn, stack_kernel)
         assert ffn.status() == 0
         ffn.close()
+
+
+@pytest.mark.parametrize("wi", [1, 3, 4])
+def test_decode_stack_tc_logits_many_tiles(P, wi):
+    """~300 owned P2 rows per CTA, all staged: more 16-row tiles than warps, each warp taking
+    whole tiles (the other shapes split a tile's k range over several warps)."""
+    w = _wl(wi, dict(d=1024, f=45600, r=256), n_layers=2)
+    layers = build_layers(w, range(w.n_layers))
+    X = make_inputs(w, 2, 1, seed=21, device="cpu").numpy()
+    ffn = _handle(P, w, [g for g, _ in layers], stack_kernel=True)
+    _stack_vs_oracle(P, w, layers, X, ffn, wi)
+    assert ffn.status() == 0
+    ffn.close()
 
 
 def test_grid_barrier_gives_up_cleanly(P):
@@ -386,7 +413,8 @@ P2_WIDE_SHAPE = dict(d=1024, f=30000, r=1024)
 @pytest.mark.parametrize("wi,shape", [(wi, STACK_SHAPE) for wi in range(5)] + [(1, P2_WIDE_SHAPE), (3, P2_WIDE_SHAPE)])
 def test_decode_stack_p2_staging_bit_identical(P, wi, shape):
     """Copying the next layer's owned P2 rows into shared memory ahead of their logits (all of
-    them, or the first ones when they do not all fit) changes nothing in the output bits."""
+    them, or the first ones when they do not all fit) changes nothing in the output bits (these
+    shapes keep the logits on the CUDA cores: r % 16 != 0, or not every row fits)."""
     w = _wl(wi, shape, n_layers=3)
     layers = build_layers(w, range(w.n_layers))
     X = make_inputs(w, 2, 1, seed=13, device="cpu").numpy()
