@@ -289,23 +289,43 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
         const StackLayer Lw = a.layers[l];
         const float *xl = l == 0 ? a.x0 : (((l - 1) & 1) ? a.xb : a.xa);
         float *xn = l == a.L - 1 ? a.x_out : ((l & 1) ? a.xb : a.xa);
-        const float inv = s_inv;
+        float inv;   // RMS scale of x_l
 
         // ------------------------------------------------------------ A: predictor hidden layer
         {
+            // The first chunks of this CTA's P1 rows (prefetched into L2 a layer ago) are requested
+            // first. x_l is staged unscaled while warp 0 adds up the slices' sums of squares, both
+            // reads in flight together; the scale is applied to the dot products (hp = ReLU(inv * P1 x)).
             constexpr int QP = VP / 4;
-            load_p1_chunk<PT>(pa, Lw.p1, k0, k1, nchp, pa_cb + lane, pa_ce);   // requested before u is staged
+            constexpr int XQ = CPT * VW / 4;   // float4 of x per thread: d <= CPT * STACK_NT * VW
+            load_p1_chunk<PT>(pa, Lw.p1, k0, k1, nchp, pa_cb + lane, pa_ce);
             if (tid < K) {   // the logits' biases, waited for before this phase's grid barrier
                 if (Lw.bp) cp_async4(&spb[tid], Lw.bp + c + P * tid);
                 else spb[tid] = 0.f;
             }
-            for (int t = tid; t < d / 4; t += STACK_NT) {
-                float4 v = __ldcg(reinterpret_cast<const float4 *>(xl) + t);
-                v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
-                const int ci = t / QP, q = t - ci * QP;
-                ua4[q * nchp + ci] = v;
+            float4 xv[XQ];
+#pragma unroll
+            for (int q = 0; q < XQ; ++q) {
+                const int t = tid + q * STACK_NT;
+                xv[q] = t < d / 4 ? __ldcg(reinterpret_cast<const float4 *>(xl) + t) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            const int nsl = (d + STACK_SLICE - 1) / STACK_SLICE;
+            float ssq = 0.f;
+            if (l > 0 && warp == 0)
+                for (int s = lane; s < nsl; s += 32) ssq += __ldcg(a.sumsq + s);
+#pragma unroll
+            for (int q = 0; q < XQ; ++q) {
+                const int t = tid + q * STACK_NT;
+                if (t >= d / 4) break;
+                const int ci = t / QP, qq = t - ci * QP;
+                ua4[qq * nchp + ci] = xv[q];
+            }
+            if (l > 0 && warp == 0) {
+                ssq = warp_sum(ssq);
+                if (lane == 0) s_inv = 1.0f / sqrtf(ssq / (float)d + a.eps);
             }
             __syncthreads();
+            inv = s_inv;
             if (l + 1 < a.L) prefetch_predictor(a.layers[l + 1]);
             const uint4 *row[8];
             const __half *srow[8];
@@ -331,7 +351,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             if (tid < 8 && k0 + tid < k1) {
                 float v = 0.f;
                 for (int w = 0; w < SNW; ++w) v += red[0][w][tid];   // fixed order
-                a.hp[k0 + tid] = fmaxf(v, 0.f);
+                a.hp[k0 + tid] = fmaxf(inv * v, 0.f);
             }
             cp_async_wait_all();
         }
@@ -769,16 +789,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 }
                 __syncthreads();
             }
-            if (l + 1 < a.L) {
-                if (!sync_grid()) return;
-                if (warp == 0) {
-                    float t = 0.f;
-                    for (int s = lane; s < nsl; s += 32) t += __ldcg(a.sumsq + s);
-                    t = warp_sum(t);
-                    if (lane == 0) s_inv = 1.0f / sqrtf(t / (float)d + a.eps);
-                }
-                __syncthreads();
-            }
+            if (l + 1 < a.L && !sync_grid()) return;
         }
     }
     // the last layer's hot copies of neurons that were not active have landed before the CTA leaves
