@@ -589,7 +589,6 @@ void plan_stack(pi_ffn_t *h)
     const size_t ring = cap - off_ring;
     h->stack_slots = (int)std::min((size_t)STACK_MAX_SLOTS, ring / slot);
     h->stack_slot_bytes = (int)slot;
-    h->stack_smem = off_ring + (size_t)h->stack_slots * slot;
     h->stack_ring = (int)((size_t)h->stack_slots * slot);
     h->off_ua = (int)off_ua;
     h->off_hp = (int)off_hp;
@@ -599,11 +598,12 @@ void plan_stack(pi_ffn_t *h)
     h->off_mbar = (int)off_mbar;
     // The ring is idle from the end of one layer's FFN to the next layer's logits: the next
     // layer's owned P2 rows are copied into it then, as many as fit (PI_FFN_STACK_P2=0: none).
+    // Between layers they may also take the rest of the shared memory past the last slot.
     const char *p2env = std::getenv("PI_FFN_STACK_P2");
-    const size_t p2row = elt_row_bytes(D.pdtype, D.r);
+    const size_t p2row = elt_row_bytes(D.pdtype, D.r), p2st = (size_t)stack_p2_stride((int)p2row);
     h->stack_p2 = 0;
-    if (!(p2env && p2env[0] == '0') && p2row % 16 == 0)
-        h->stack_p2 = (int)std::min(own, (size_t)h->stack_ring / (size_t)stack_p2_stride((int)p2row));
+    if (!(p2env && p2env[0] == '0') && p2row % 16 == 0) h->stack_p2 = (int)std::min(own, ring / p2st);
+    h->stack_smem = off_ring + std::max((size_t)h->stack_ring, (size_t)h->stack_p2 * p2st);
     h->stack_ok = true;
 }
 

@@ -43,6 +43,7 @@ namespace pi {
 
 constexpr int SNW = STACK_NT / 32;
 static_assert(SNW == 16, "the batch reduction maps the 16 warps onto half a warp's lanes");
+static_assert(STACK_MAX_CHUNK <= STACK_NT, "one owned neuron per thread");
 
 template <int WT>
 __host__ __device__ constexpr int weight_row_bytes(int d)
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     __shared__ int s_flag;
     __shared__ uint64_t s_p2bar;   // the staged P2 rows of the next layer have landed
     __shared__ float spb[STACK_MAX_CHUNK];   // predictor bias of the owned rows, copied during phase A
+    __shared__ const void *s_p2next;          // P2 of the next layer (read during phase A)
     __shared__ int s_pend[2];      // thread 0: parity of staged P2 copies not yet waited for, of the
                                    // last hot-slot copies issued (-1: none)
 
@@ -216,10 +218,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     auto expect_p2 = [&]() {
         if (tid == 0) mbar_arrive_expect_tx(&s_p2bar, (uint32_t)((KS - ks0) * p2b));
     };
-    auto stage_p2 = [&](const StackLayer &L) {   // one copy per thread; the ring is free and expect_p2 ran
+    auto stage_p2 = [&](const void *p2) {   // one copy per thread; the ring is free and expect_p2 ran
         if (tid >= ks0 && tid < KS) {
             fence_proxy_async_smem();
-            bulk_g2s(ring + (size_t)tid * p2st, (const char *)L.p2 + (size_t)(c + (size_t)P * tid) * p2b, (uint32_t)p2b,
+            bulk_g2s(ring + (size_t)tid * p2st, (const char *)p2 + (size_t)(c + (size_t)P * tid) * p2b, (uint32_t)p2b,
                      &s_p2bar);
         }
     };
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     prefetch_predictor(a.layers[0]);
     __syncthreads();
     issue_hot(a.layers[0], -1);
-    if (KS > 0) stage_p2(a.layers[0]);
+    if (KS > 0) stage_p2(a.layers[0].p2);
     if (a.idx_out)
         for (int i = c * STACK_NT + tid; i < a.L * W; i += P * STACK_NT) a.maskw[i] = 0u;
     if (a.counts && c == 0)
@@ -298,11 +300,6 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             // reads in flight together; the scale is applied to the dot products (hp = ReLU(inv * P1 x)).
             constexpr int QP = VP / 4;
             constexpr int XQ = CPT * VW / 4;   // float4 of x per thread: d <= CPT * STACK_NT * VW
-            load_p1_chunk<PT>(pa, Lw.p1, k0, k1, nchp, pa_cb + lane, pa_ce);
-            if (tid < K) {   // the logits' biases, waited for before this phase's grid barrier
-                if (Lw.bp) cp_async4(&spb[tid], Lw.bp + c + P * tid);
-                else spb[tid] = 0.f;
-            }
             float4 xv[XQ];
 #pragma unroll
             for (int q = 0; q < XQ; ++q) {
@@ -313,6 +310,12 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             float ssq = 0.f;
             if (l > 0 && warp == 0)
                 for (int s = lane; s < nsl; s += 32) ssq += __ldcg(a.sumsq + s);
+            load_p1_chunk<PT>(pa, Lw.p1, k0, k1, nchp, pa_cb + lane, pa_ce);   // after x: its reads come back first
+            if (tid < K) {   // the logits' biases, waited for before this phase's grid barrier
+                if (Lw.bp) cp_async4(&spb[tid], Lw.bp + c + P * tid);
+                else spb[tid] = 0.f;
+            }
+            if (tid == STACK_NT - 1 && l + 1 < a.L) s_p2next = a.layers[l + 1].p2;
 #pragma unroll
             for (int q = 0; q < XQ; ++q) {
                 const int t = tid + q * STACK_NT;
@@ -408,6 +411,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             // hi + lo halves in the predictor's type (so ~16 bits of it, with fp32 accumulation).
             bool tcl = false;
             if constexpr (PT == DT_BF16 || PT == DT_F16) tcl = KS == K && K > 0 && (r & 15) == 0;
+            bool act = false;   // owned neuron k = tid fires
             if (tcl) {
                 uint32_t *bfr = reinterpret_cast<uint32_t *>(hp4);   // B fragments [r/16][8 lanes][2]
 #pragma unroll
@@ -436,26 +440,32 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     const int s0 = g * NKS / G, s1 = (g + 1) * NKS / G;
                     const int rw = min(t * 16 + (lane & 15), K - 1);   // rows past K repeat row K - 1
                     const uint32_t ab = smem_u32(ring) + (uint32_t)(rw * p2st) + (uint32_t)(lane >> 4) * 16u;
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int s16 = s0; s16 < s1; ++s16) {
-                        uint32_t af[4];
-                        ldsm_x4(ab + (uint32_t)s16 * 32u, af);
-                        const uint2 bf =
-                            lane < 8 ? reinterpret_cast<const uint2 *>(bfr)[s16 * 8 + lane] : make_uint2(0u, 0u);
-                        mma_16816<PT>(acc, af, bf.x, bf.y);
+                    // two accumulators (even and odd k steps), so consecutive products do not wait
+                    // on each other
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    for (int s16 = s0; s16 < s1; s16 += 2) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            if (s16 + e >= s1) break;
+                            uint32_t af[4];
+                            ldsm_x4(ab + (uint32_t)(s16 + e) * 32u, af);
+                            const uint2 bf = lane < 8 ? reinterpret_cast<const uint2 *>(bfr)[(s16 + e) * 8 + lane]
+                                                      : make_uint2(0u, 0u);
+                            mma_16816<PT>(acc[e], af, bf.x, bf.y);
+                        }
                     }
                     if ((lane & 3) == 0) {   // columns 0 (hi part) and 1 (lo part) of rows lane/4, lane/4 + 8
-                        zp[u * 16 + (lane >> 2)] = acc[0] + acc[1];
-                        zp[u * 16 + (lane >> 2) + 8] = acc[2] + acc[3];
+                        zp[u * 16 + (lane >> 2)] = (acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1]);
+                        zp[u * 16 + (lane >> 2) + 8] = (acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3]);
                     }
                 }
                 __syncthreads();
-                for (int k = tid; k < K; k += STACK_NT) {
-                    const int t = k >> 4;
+                if (tid < K) {
+                    const int t = tid >> 4;
                     float z = 0.f;
-                    for (int g = 0; g < G; ++g) z += zp[(t * G + g) * 16 + (k & 15)];   // fixed order
-                    z += spb[k];
-                    sflag[k] = (c + P * k < a.hot_prefix || z > a.tau) ? 1 : 0;
+                    for (int g = 0; g < G; ++g) z += zp[(t * G + g) * 16 + (tid & 15)];   // fixed order
+                    z += spb[tid];
+                    act = c + P * tid < a.hot_prefix || z > a.tau;
                 }
             } else {
                 rows_at(warp);
@@ -487,34 +497,26 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                         if (lane == 0 && k < K) sflag[k] = (i < a.hot_prefix || z > a.tau) ? 1 : 0;
                     }
                 }
+                __syncthreads();
+                act = tid < K && sflag[tid];
             }
-            __syncthreads();
-            // ascending list of the owned active neurons
-            const int per = (K + STACK_NT - 1) / STACK_NT;
-            const int ka = min(K, tid * per), kz = min(K, ka + per);
-            int mine = 0;
-            for (int k = ka; k < kz; ++k) mine += sflag[k];
-            int incl = mine;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            if (lane == 31) wsum[warp] = incl;
+            // ascending list of the owned active neurons (thread k holds owned neuron k's flag)
+            const uint32_t bal = __ballot_sync(0xffffffffu, act);
+            if (lane == 0) wsum[warp] = __popc(bal);
             __syncthreads();
             int before = 0, nn = 0;
             for (int w = 0; w < SNW; ++w) {
-                before += w < warp ? wsum[w] : 0;
-                nn += wsum[w];
+                const int v = wsum[w];
+                before += w < warp ? v : 0;
+                nn += v;
             }
-            int off = before + incl - mine;
-            for (int k = ka; k < kz; ++k)
-                if (sflag[k]) {
-                    const int i = c + P * k;
-                    if (!bias_bulk) sbias[off] = Lw.bg ? __ldg(Lw.bg + i) : 0.f;
-                    sneur[off++] = i;
-                    if (a.idx_out) atomicOr(a.maskw + (size_t)l * W + (i >> 5), 1u << (i & 31));
-                }
+            if (act) {
+                const int off = before + __popc(bal & ((1u << lane) - 1u));
+                const int i = c + P * tid;
+                if (!bias_bulk) sbias[off] = Lw.bg ? __ldg(Lw.bg + i) : 0.f;
+                sneur[off] = i;
+                if (a.idx_out) atomicOr(a.maskw + (size_t)l * W + (i >> 5), 1u << (i & 31));
+            }
             if (tid == 0 && a.counts && nn) atomicAdd(a.counts + l, nn);
             __syncthreads();
 
@@ -726,7 +728,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             if (l + 1 < a.L && KS > 0) {
                 expect_p2();
                 __syncthreads();
-                stage_p2(a.layers[l + 1]);
+                stage_p2(s_p2next);
                 if (tid == 0) s_pend[0] = (l + 1) & 1;
             }
         }
