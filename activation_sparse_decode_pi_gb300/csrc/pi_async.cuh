@@ -147,15 +147,23 @@ struct PendingCopies {
     const int *par;
 };
 
+struct NoWork {
+    __device__ void operator()() const {}
+};
+
 // Returns false in every thread of a CTA that gave up waiting (after recording PI_ERR_TIMEOUT
-// and waiting, bounded, for the copies `pc` names to land).
+// and waiting, bounded, for the copies `pc` names to land). Every thread runs `work` between
+// the CTA's arrival and its wait: work no other CTA waits for, such as issuing copies into
+// this CTA's own shared memory.
+template <typename Work = NoWork>
 __device__ __forceinline__ bool grid_sync_to(unsigned long long *cnt, unsigned long long target, uint32_t *status,
-                                             int *s_flag, const PendingCopies *pc = nullptr)
+                                             int *s_flag, const PendingCopies *pc = nullptr, Work work = Work())
 {
     __syncthreads();
+    if (threadIdx.x == 0) red_release_add_u64(cnt, 1ull);   // release: the CTA's writes before the CTA barrier
+    work();
     if (threadIdx.x == 0) {
         int ok = 1;
-        red_release_add_u64(cnt, 1ull);   // release: the CTA's writes before the CTA barrier
         if ((long long)(ld_acquire_u64(cnt) - target) < 0) {
             const unsigned long long t0 = globaltimer_ns();
             while ((long long)(ld_acquire_u64(cnt) - target) < 0) {

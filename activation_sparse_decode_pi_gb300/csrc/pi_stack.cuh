@@ -210,18 +210,22 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     // slot HK + n % SC with parity (n / SC) & 1.
     uint32_t cseq = 0;
     unsigned kb = 0;    // grid barriers passed in this launch
-    auto sync_grid = [&]() -> bool {
+    auto sync_grid = [&](auto work) -> bool {
         ++kb;
         const PendingCopies pc{&s_p2bar, mbar, min(a.hot_k, K), s_pend};
-        return grid_sync_to(a.bar, s_base + (unsigned long long)kb * a.nblocks, a.status, &s_flag, &pc);
+        return grid_sync_to(a.bar, s_base + (unsigned long long)kb * a.nblocks, a.status, &s_flag, &pc, work);
     };
+    const NoWork no_work;
     auto expect_p2 = [&]() {
         if (tid == 0) mbar_arrive_expect_tx(&s_p2bar, (uint32_t)((KS - ks0) * p2b));
     };
-    auto stage_p2 = [&](const void *p2) {   // one copy per thread; the ring is free and expect_p2 ran
-        if (tid >= ks0 && tid < KS) {
+    // one copy per thread, row k = 16 * lane + warp (a warp's copies are issued one after another,
+    // so every warp takes a few); the ring is free and expect_p2 ran
+    auto stage_p2 = [&](const void *p2) {
+        const int k = lane * SNW + warp;
+        if (k >= ks0 && k < KS) {
             fence_proxy_async_smem();
-            bulk_g2s(ring + (size_t)tid * p2st, (const char *)p2 + (size_t)(c + (size_t)P * tid) * p2b, (uint32_t)p2b,
+            bulk_g2s(ring + (size_t)k * p2st, (const char *)p2 + (size_t)(c + (size_t)P * k) * p2b, (uint32_t)p2b,
                      &s_p2bar);
         }
     };
@@ -285,7 +289,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             s_inv = 1.0f / sqrtf(s / (float)d + a.eps);
         }
     }
-    if (!sync_grid()) return;
+    if (!sync_grid(no_work)) return;
 
     for (int l = 0; l < a.L; ++l) {
         const StackLayer Lw = a.layers[l];
@@ -358,7 +362,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             }
             cp_async_wait_all();
         }
-        if (!sync_grid()) return;
+        if (!sync_grid(no_work)) return;
 
         // ------------------------------------------------------------ BC: logits, then the sparse FFN
         {
@@ -717,22 +721,22 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     reinterpret_cast<float4 *>(pq + (size_t)ci * VW)[e4] =
                         make_float4(yr[cc][4 * e4], yr[cc][4 * e4 + 1], yr[cc][4 * e4 + 2], yr[cc][4 * e4 + 3]);
             }
-            // every thread is done with the ring: the next layer's hot rows can be requested now,
-            // a whole layer before their predictor runs
-            if (l + 1 < a.L && a.hot_k > 0) {
-                __syncthreads();
-                issue_hot(a.layers[l + 1], l);
-                if (tid == 0) s_pend[1] = (l + 1) & 1;
-            }
-            // likewise the next layer's staged P2 rows
-            if (l + 1 < a.L && KS > 0) {
-                expect_p2();
-                __syncthreads();
-                stage_p2(s_p2next);
-                if (tid == 0) s_pend[0] = (l + 1) & 1;
+        }
+        // Once every thread is done with the ring (the barrier's CTA sync), the next layer's hot
+        // rows (a whole layer before their predictor runs) or its staged P2 rows are requested
+        // while this CTA waits for the others.
+        if (l + 1 < a.L) {
+            if (KS > 0) expect_p2();
+            if (tid == 0) {
+                if (a.hot_k > 0) s_pend[1] = (l + 1) & 1;
+                if (KS > 0) s_pend[0] = (l + 1) & 1;
             }
         }
-        if (!sync_grid()) return;
+        if (!sync_grid([&] {
+                if (l + 1 < a.L && a.hot_k > 0) issue_hot(a.layers[l + 1], l);
+                if (l + 1 < a.L && KS > 0) stage_p2(s_p2next);
+            }))
+            return;
 
         // ------------------------------------------------------------ D: fixed-order reduction + residual
         {
@@ -791,7 +795,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 }
                 __syncthreads();
             }
-            if (l + 1 < a.L && !sync_grid()) return;
+            if (l + 1 < a.L && !sync_grid(no_work)) return;
         }
     }
     // the last layer's hot copies of neurons that were not active have landed before the CTA leaves
