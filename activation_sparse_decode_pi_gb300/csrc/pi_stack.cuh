@@ -159,6 +159,40 @@ __device__ __forceinline__ void stage_neuron(const StackArgs &a, const StackLaye
     if (a.bias_bulk) bulk_g2s(sl + bias_off, Lw.bg + (i & ~3), 16, mb);
 }
 
+// Copies that make up one neuron's slot: its weight rows, (int4) their scale rows, and the
+// 16-byte chunk holding its gate bias when biases travel with the rows.
+template <int WT, int KIND>
+__device__ __forceinline__ int stage_parts(const StackArgs &a)
+{
+    constexpr int ROWS = KIND == KIND_GATED ? 3 : 2;
+    return ROWS * (WT == DT_INT4 ? 2 : 1) + (a.bias_bulk ? 1 : 0);
+}
+
+// Copy j (< stage_parts) of neuron i's slot; copy 0 also registers the slot's byte count. The
+// copies of one slot may be issued by different threads in any order.
+template <int WT, int KIND>
+__device__ __forceinline__ void stage_part(const StackArgs &a, const StackLayer &Lw, unsigned char *ring,
+                                           uint64_t *mbar, int slot, int i, int j)
+{
+    constexpr int ROWS = KIND == KIND_GATED ? 3 : 2;
+    const int rowb = WT == DT_F32 ? a.d * 4 : (WT == DT_INT4 ? a.d / 2 : a.d * 2);
+    const int sclb = WT == DT_INT4 ? (a.d / 128) * 2 : 0;
+    const int bias_off = ROWS * (rowb + sclb);
+    unsigned char *sl = ring + (size_t)slot * a.slot_bytes;
+    uint64_t *mb = &mbar[slot];
+    if (j == 0) mbar_arrive_expect_tx(mb, (uint32_t)(bias_off + (a.bias_bulk ? 16 : 0)));
+    if (j < ROWS) {
+        const void *src = j == 0 ? Lw.wg : (KIND == KIND_GATED && j == 1 ? Lw.wu : Lw.wd);
+        bulk_g2s(sl + j * rowb, (const char *)src + (size_t)i * rowb, rowb, mb);
+    } else if (WT == DT_INT4 && j < 2 * ROWS) {
+        const int q = j - ROWS;
+        const void *src = q == 0 ? Lw.sg : (KIND == KIND_GATED && q == 1 ? Lw.su : Lw.sd);
+        bulk_g2s(sl + ROWS * rowb + q * sclb, (const char *)src + (size_t)i * sclb, sclb, mb);
+    } else {
+        bulk_g2s(sl + bias_off, Lw.bg + (i & ~3), 16, mb);
+    }
+}
+
 template <int WT, int PT, int KIND, int CPT>
 __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 {
@@ -537,13 +571,14 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 par = (sq / (uint32_t)SC) & 1u;
                 return HK + (int)(sq % (uint32_t)SC);
             };
-            // the first cold neurons, one issuing thread per neuron (lane 0 of warp (m - nh) % SNW)
-            if (lane == 0 && nh + warp < nn) {
+            // the first cold neurons' copies: copy q goes to lane q / 16 of warp q % 16 (a warp
+            // issues its copies one after another, so every warp takes a few)
+            const int NPART = stage_parts<WT, KIND>(a);
+            const int cq = lane * SNW + warp, cw = cq / NPART, cj = cq - cw * NPART;   // this thread's copy
+            if (nh + cw < nn && cw < SC) {
                 fence_proxy_async_smem();
-                for (int m = nh + warp; m < nn && m < nh + SC; m += SNW) {
-                    uint32_t par;
-                    stage_neuron<WT, KIND>(a, Lw, ring, mbar, slot_of(m, par), sneur[m]);
-                }
+                uint32_t par;
+                stage_part<WT, KIND>(a, Lw, ring, mbar, slot_of(nh + cw, par), sneur[nh + cw], cj);
             }
             // this thread's columns of u, scaled (loaded while the first rows are in flight)
             float ur[CPT][VW];
@@ -657,14 +692,12 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     return;
                 }
                 // the previous cold batch's slots are free: entry k + SC takes entry k's slot
-                if (cold && m0 - nbc >= nh && lane == 0 && warp < nbc) {
-                    const int k = m0 - nbc + warp;
-                    if (k + SC < nn) {
-                        fence_proxy_async_smem();
-                        int sk = (int)cs - nbc + warp;
-                        if (sk < 0) sk += SC;
-                        stage_neuron<WT, KIND>(a, Lw, ring, mbar, HK + sk, sneur[k + SC]);
-                    }
+                // (copy j of the batch's w-th refill goes to the thread that took copy j of cold entry w)
+                if (cold && m0 - nbc >= nh && cw < nbc && m0 - nbc + cw + SC < nn) {
+                    fence_proxy_async_smem();
+                    int sk = (int)cs - nbc + cw;
+                    if (sk < 0) sk += SC;
+                    stage_part<WT, KIND>(a, Lw, ring, mbar, HK + sk, sneur[m0 - nbc + cw + SC], cj);
                 }
 #pragma unroll
                 for (int k = 0; k < NB; ++k) {
