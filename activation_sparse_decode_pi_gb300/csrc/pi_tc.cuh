@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
     __shared__ uint32_t tmem_base;
     __shared__ volatile int s_abort;    // any role gave up: the others stop early
     __shared__ volatile int s_dabort;   // written by drain threads only, read after a drain barrier
-    __shared__ int s_last, s_wsum[4];
+    __shared__ int s_last, s_wsum[TC_THREADS / 32];
+    __shared__ int s_compact;           // this CTA completed the last logits tile: it lists the active rows
 
     const uint32_t sbase = (smem_u32(dsm) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
         mbar_init(&fin, 1);
         s_abort = 0;
         s_dabort = 0;
+        s_compact = 0;
         fence_mbar_init();
     }
     if (warp == TC_MMA_WARP) tmem_alloc(&tmem_base, TCOLS);
@@ -499,16 +501,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_tc(const TcArgs a)
                     const uint32_t word = __ballot_sync(0xffffffffu, act);
                     const int wi = (a.row0 + t * 128 + 32 * warp) >> 5;
                     if (lane == 0 && wi < nwords) a.maskw[wi] = word;
-                    named_sync(1, 128);
-                    if (threadIdx.x == 0) s_last = atom_add_acq_rel(a.done_cnt, 1u) == (unsigned)tiles - 1;
-                    named_sync(1, 128);
-                    if (s_last) {
-                        compact_words<4>(a.maskw, nwords, a.row0 / 32, a.idx_out, a.count_out, s_wsum,
-                                         [] { named_sync(1, 128); });
-                        if (threadIdx.x == 0) *a.done_cnt = 0u;
-                    }
+                    named_sync(1, 128);   // the four warps' mask words before the releasing ticket
+                    if (threadIdx.x == 0 && atom_add_acq_rel(a.done_cnt, 1u) == (unsigned)tiles - 1) s_compact = 1;
                 }
             }
+        }
+    }
+
+    // ---- the CTA that completed the last logits tile lists the active rows, with every warp
+    if constexpr (MODE == TC_LOGITS) {
+        __syncthreads();
+        if (s_compact) {
+            compact_words<TC_THREADS / 32>(a.maskw, (a.f + 31) / 32, a.row0 / 32, a.idx_out, a.count_out, s_wsum,
+                                           [] { __syncthreads(); });
+            if (threadIdx.x == 0) *a.done_cnt = 0u;
         }
     }
 
