@@ -573,10 +573,14 @@ void plan_stack(pi_ffn_t *h)
     const size_t sclb = D.wdtype == PI_INT4_G128 ? (size_t)(D.d / 128) * 2 : 0;
     const size_t slot = align_up(rows * (rowb + sclb) + 16, 128);
     const size_t own = (size_t)(D.f + P - 1) / P;
+    // u (phase A), hp (phase BC) and the reduction scratch (BC and D) are never live together
+    // with u: hp and the scratch share u's region when they fit in it.
     const size_t off_ua = 0;
-    const size_t off_hp = align_up(off_ua + (size_t)D.d * 4, 128);
+    const size_t ua_end = align_up((size_t)D.d * 4, 128);
+    const bool share = align_up((size_t)D.r * 4, 128) + 8192 <= ua_end;
+    const size_t off_hp = share ? off_ua : ua_end;
     const size_t off_scr = align_up(off_hp + (size_t)D.r * 4, 128);
-    const size_t off_flags = off_scr + 8192;
+    const size_t off_flags = share ? ua_end : off_scr + 8192;
     const size_t off_mbar = align_up(off_flags + own, 16);
     const size_t off_ring = align_up(off_mbar + 8 * STACK_MAX_SLOTS, 128);
     int optin = 0;
