@@ -145,6 +145,7 @@ struct pi_ffn {
     int tc_stages[5][4][2] = {};       // [mode][log2(NB / 16)][log2(w)]
     size_t tc_smem[5][4][2] = {};
     int tc_kw = 1, tc_ds = 1, tc_stage_cap = TC_MAX_STAGES;   // tuning (PI_FFN_TC_KW / _DS / _STAGES)
+    int tc_hidden_cpt = 8;             // CTAs per predictor-hidden tile (PI_FFN_TC_HIDDEN_CPT)
     uint16_t *tc_uhi = nullptr, *tc_ulo = nullptr, *tc_hphi = nullptr, *tc_hplo = nullptr, *tc_hhi = nullptr,
              *tc_hlo = nullptr;
     float *tc_part = nullptr;
@@ -321,6 +322,7 @@ void plan_tc(pi_ffn_t *h)
     };
     h->tc_kw = env_int("PI_FFN_TC_KW", 2) >= 2 ? 2 : 1;
     h->tc_ds = env_int("PI_FFN_TC_DS", 2) >= 2 ? 2 : 1;
+    h->tc_hidden_cpt = std::max(1, env_int("PI_FFN_TC_HIDDEN_CPT", 8));
     h->tc_stage_cap = std::min(TC_MAX_STAGES, env_int("PI_FFN_TC_STAGES", TC_MAX_STAGES));
     const size_t avail = (size_t)optin > 2048 ? (size_t)optin - 2048 : 0;   // alignment slack + static barriers
     for (int mode = 0; mode < 5; ++mode)
@@ -384,8 +386,14 @@ cudaError_t tc_launch(const pi_ffn_t *h, int mode, int nb, const TcArgs &a0, cud
     a.done_cnt = h->tc_cnt + h->tc_ntiles;
     a.status = h->status;
     const size_t smem = h->tc_smem[mode][i][wi];
-    return h->desc.wdtype == PI_BF16 ? tc_dispatch<1>(mode, nb, w, a, h->nsm, smem, s, pdl)
-                                     : tc_dispatch<2>(mode, nb, w, a, h->nsm, smem, s, pdl);
+    // The predictor's hidden layer has few tiles (r / 128) and a long K: spread over every SM,
+    // each tile's k range is cut into ~19 parts whose partials one CTA adds at the end. A few
+    // CTAs per tile stream the same bytes with far fewer partials to add.
+    int grid = h->nsm;
+    if (mode == TC_PRED_HIDDEN && a.count == nullptr)
+        grid = std::min(h->nsm, std::max(1, (a.n_static + 127) / 128) * h->tc_hidden_cpt);
+    return h->desc.wdtype == PI_BF16 ? tc_dispatch<1>(mode, nb, w, a, grid, smem, s, pdl)
+                                     : tc_dispatch<2>(mode, nb, w, a, grid, smem, s, pdl);
 }
 
 // u (or x_l with rms) -> uhi, ulo [NB x d]
