@@ -6,15 +6,17 @@
 // 512 threads that walks all layers. A layer is three phases separated by bounded
 // grid barriers:
 //
-//   A   hp[k] = ReLU(u . P1T[k])            CTA c: hidden units [c*r/P, (c+1)*r/P)
+//   A   hp[k] = ReLU(inv * P1T[k] . x)      CTA c: hidden units [c*r/P, (c+1)*r/P); x is
+//       staged unscaled while the RMS scale inv is summed from the slices' sums of squares
 //   -- barrier
 //   BC  CTA c owns the neurons i = c, c+P, c+2P, ... (hot-first order spreads the hot
 //       neurons evenly). It computes their logits z[i] = hp . P2T[i] + b_p[i], keeps the
 //       ones with z > tau in ascending order, bulk-copies their gate(/up) and W_down rows
 //       and gate bias into a shared-memory ring (cp.async.bulk + mbarrier), reduces
-//       h = ReLU(u.Wg + bg) * (u.Wu) over the CTA a few neurons at a time, and accumulates
-//       h * WdT into fp32 registers (each thread owns fixed columns). One partial per CTA.
-//   -- barrier
+//       h = ReLU(u.Wg + bg) * (u.Wu) over the CTA up to four neurons at a time, and
+//       accumulates h * WdT into fp32 registers (each thread owns fixed columns). One
+//       partial per CTA.
+//   -- barrier (while waiting, the CTA requests the next layer's owned P2 rows into its ring)
 //   D   x_{l+1} = x_l + sum of the P partials in a fixed order, per 32-column slice, plus
 //       that slice's sum of squares for the next layer's RMS scale.
 //   -- barrier
@@ -22,12 +24,15 @@
 // Neither a global mask scan nor a global active list is on the critical path: each
 // CTA computes the FFN of exactly the neurons whose logits it computed. The active
 // counts (and, on request, the ascending active lists) are produced alongside.
-// The predictor weights do not depend on the input: each CTA prefetches its predictor
-// slice of the next layer into L2 while the current layer runs, and requests its P1
-// rows before it stages u.
+// The predictor weights do not depend on the input. The ring is idle between one layer's
+// FFN and the next layer's logits, so the next layer's owned P2 rows are copied into it
+// then (as many as fit); the logits of a CTA whose rows all fit run as 16-row tiles on the
+// tensor cores (mma.sync, hp split into hi and lo halves of the predictor's type), the
+// others as CUDA-core row dot products. P1 and the P2 rows that do not fit are prefetched
+// into L2 a layer ahead.
 // Hot neurons (the first hot_k owned ones in hot-first order, typically active on most
-// tokens) have ring slots of their own: their rows are requested one layer ahead, during the
-// previous layer's reduction phase, before the predictor has said whether they fire. A hot
+// tokens) can have ring slots of their own: their rows are requested one layer ahead, during
+// the previous layer's barrier wait, before the predictor has said whether they fire. A hot
 // neuron the predictor rejects costs its bytes and nothing else: the neurons are reduced in
 // the same list order either way, so the output bits do not depend on hot_k.
 // The result is deterministic: every sum runs in a fixed order for a given grid size.

@@ -145,7 +145,9 @@ pi_status_t pi_sparse_ffn(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
  * persistent cooperative kernel, one CTA per SM, whose layers are separated by bounded
  * grid barriers; a barrier that gives up records PI_ERR_TIMEOUT. Its partial sums are
  * one per CTA, so the output bits depend on the SM count (and nothing else).
- * PI_FFN_STACK_KERNEL=0 in the environment at pi_ffn_create turns it off. Other steps
+ * PI_FFN_STACK_KERNEL=0 in the environment at pi_ffn_create turns it off;
+ * PI_FFN_STACK_P2=0 keeps the predictor's P2 rows out of its shared memory (the logits
+ * then run on the CUDA cores from L2). Other steps
  * run as a chain of kernels, recorded once outside stream capture into a CUDA graph
  * per (B, pointer set) and replayed.
  */
