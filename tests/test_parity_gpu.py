@@ -280,6 +280,8 @@ def _handle(P, w, layers, stack_kernel: bool):
 STACK_SHAPE_TC = dict(d=2048, f=3001, r=144)
 # d * 4 bytes >= r * 4 + 8 KB: hp and the reduction scratch share u's shared-memory region
 STACK_SHAPE_SHARED = dict(d=4096, f=3001, r=256)
+# fewer neurons than SMs: most CTAs own one neuron (a one-row logit tile) or none
+STACK_SHAPE_FEW = dict(d=1024, f=100, r=64)
 
 
 def _stack_vs_oracle(P, w, layers, X, ffn, tag):
@@ -308,7 +310,8 @@ def _stack_vs_oracle(P, w, layers, X, ffn, tag):
             assert err <= TOL[w.wdtype], (tag, err)
 
 
-@pytest.mark.parametrize("shape", [STACK_SHAPE, STACK_SHAPE_TC, STACK_SHAPE_SHARED], ids=["r136", "r144", "d4096"])
+@pytest.mark.parametrize("shape", [STACK_SHAPE, STACK_SHAPE_TC, STACK_SHAPE_SHARED, STACK_SHAPE_FEW],
+                         ids=["r136", "r144", "d4096", "f100"])
 @pytest.mark.parametrize("wi", range(5))
 def test_decode_stack_both_paths_batch1(P, wi, shape):
     """Batch 1: the single persistent kernel and the multi-kernel step both match the oracle."""
