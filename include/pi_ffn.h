@@ -29,6 +29,19 @@
  *    outside [0, f]) are recorded in a device status word and the offending
  *    entry is skipped; pi_get_status() reports them. No kernel traps.
  *  - No C++ exception crosses this boundary. Not thread-safe per handle.
+ *
+ * Environment, read at pi_ffn_create (all optional; the defaults are the tuned paths):
+ *  - PI_FFN_STACK_KERNEL=0  batch-1 steps use the multi-kernel chain instead of the
+ *                           persistent one-kernel step.
+ *  - PI_FFN_STACK_P2=0      the persistent step reads the predictor's P2 rows from L2
+ *                           instead of staging them in shared memory.
+ *  - PI_FFN_TC=0            batch >= 16 stays on the CUDA-core kernels.
+ *  - PI_FFN_TC_MIN_BATCH=n  smallest batch for the tensor-core path (default 16).
+ *  - PI_FFN_TC_KW, PI_FFN_TC_DS, PI_FFN_TC_STAGES, PI_FFN_TC_HIDDEN_CPT: tensor-core step
+ *    widths (64-wide K blocks per step, 128-column W_down slices per tile: 1 or 2, default
+ *    2), ring depth cap, and CTAs per predictor-hidden tile (default 8).
+ * They change speed and, for some, the order of floating-point additions (so the output
+ * bits), not what is computed.
  */
 #ifndef PI_FFN_H
 #define PI_FFN_H
