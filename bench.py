@@ -68,9 +68,15 @@ def csrc_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(w, kernel: str):
+def ncu_traffic(w, kernel: str, B: int = 1, hot_prefix: int = 0, n_hot: int = 0):
+    """DRAM bytes per launch from the recorded ncu capture, scaled by the layer count; None
+    unless the run is the captured configuration (the workload's own shape, batch 1, no hot
+    prefix or hot slots) on the captured kernel sources."""
     rec = NCU_TRAFFIC.get((w.name, kernel))
     if not rec or not rec["bytes_per_layer"] or kernel not in KERNEL_SOURCES or rec["csrc"] != csrc_hash(kernel):
+        return None
+    base = WORKLOADS[w.name]
+    if (w.d, w.f, w.r) != (base.d, base.f, base.r) or B != 1 or hot_prefix or n_hot:
         return None
     return rec["bytes_per_layer"] * w.n_layers
 
@@ -425,7 +431,7 @@ def run_ours(args):
         "predictor_time_share": ((kinds.get("pred_hidden", (0.0, 0))[0] + kinds.get("pred_logits", (0.0, 0))[0]) /
                                  sum(v[0] for v in kinds.values())) if ("pred_hidden" in kinds) else None,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": ncu_traffic(w, dom), "algorithmic_bytes": dom_bytes,
+                     "frac": achieved / peak, "traffic": ncu_traffic(w, dom, B, hot_prefix, n_hot), "algorithmic_bytes": dom_bytes,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s"},
         "kernels": kernel_table,

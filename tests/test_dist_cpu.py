@@ -65,3 +65,29 @@ def test_step_bytes_accounting():
     w5 = WORKLOADS["opt175b_d12288_f49152_int4_L96"]
     assert bench.neuron_bytes(w5) == 2 * 12288 // 2 + 4 + 2 * (12288 // 128) * 2
     assert bench.kernel_bytes(w5, "pred_logits", 0, 1) == 49152 * 1024 * 2 + 49152 * 4
+
+
+def test_ncu_traffic_only_for_the_captured_configuration():
+    """The recorded DRAM traffic is reported only for the captured configuration: the
+    workload's own shape at batch 1, no hot prefix or hot slots, the captured sources;
+    it scales with the layer count."""
+    import dataclasses
+
+    import bench
+    from workload import WORKLOADS
+
+    name = "relullama7b_d4096_f11008_bf16_L32"
+    w = WORKLOADS[name]
+    rec = bench.NCU_TRAFFIC[(name, "decode_stack")]
+    if rec["csrc"] == bench.csrc_hash("decode_stack"):
+        assert bench.ncu_traffic(w, "decode_stack") == pytest.approx(rec["bytes_per_layer"] * 32)
+        assert bench.ncu_traffic(dataclasses.replace(w, n_layers=4), "decode_stack") == pytest.approx(
+            rec["bytes_per_layer"] * 4)
+    else:   # sources changed since the capture: no traffic figure
+        assert bench.ncu_traffic(w, "decode_stack") is None
+    assert bench.ncu_traffic(dataclasses.replace(w, r=128), "decode_stack") is None
+    assert bench.ncu_traffic(w, "decode_stack", B=4) is None
+    assert bench.ncu_traffic(w, "decode_stack", hot_prefix=100) is None
+    assert bench.ncu_traffic(w, "decode_stack", n_hot=100) is None
+    assert bench.ncu_traffic(w, "ffn_down") is None
+    assert bench.ncu_traffic(WORKLOADS["llama2_13b_d5120_f13824_bf16_L40"], "decode_stack") is None
