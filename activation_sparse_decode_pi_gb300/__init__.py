@@ -35,8 +35,12 @@ EXPORTS = (
     "pi_ffn_create", "pi_ffn_destroy", "pi_predict", "pi_sparse_ffn", "pi_decode_stack",
     "pi_hot_first_order", "pi_permute_rows", "pi_get_status", "pi_status_string", "pi_abi_version",
     "pi_profile_begin", "pi_profile_end", "pi_sparse_ffn_noalloc", "pi_selftest_grid_barrier",
-    "pi_selftest_umma", "pi_ffn_set_hot_neurons", "pi_ffn_set_hot_prefix",
+    "pi_selftest_umma", "pi_ffn_set_hot_neurons", "pi_ffn_set_hot_prefix", "pi_decode_stack_layers",
+    "pi_ffn_set_phase_trace",
 )
+PI_STACK_PHASES = 8
+STACK_PHASE_NAMES = ("layer_start", "hidden_done", "logits_start", "list_ready", "first_rows", "ffn_done",
+                     "reduce_start", "reduce_done")
 PI_NOALLOC_SCRATCH_BYTES = 16 << 20
 KERNEL_KINDS = ("rms", "pred_hidden", "pred_logits", "ffn_h", "ffn_down", "reduce", "decode_stack")
 
@@ -67,6 +71,10 @@ _lib.pi_sparse_ffn.restype = ctypes.c_int
 _lib.pi_sparse_ffn.argtypes = [_P, _I32, _P, _I32, _P, _P, _P, _P]
 _lib.pi_decode_stack.restype = ctypes.c_int
 _lib.pi_decode_stack.argtypes = [_P, _P, _I32, _P, _P, _P, _P]
+_lib.pi_decode_stack_layers.restype = ctypes.c_int
+_lib.pi_decode_stack_layers.argtypes = [_P, _P, _I32, _P, _P, _P, _P, _P]
+_lib.pi_ffn_set_phase_trace.restype = ctypes.c_int
+_lib.pi_ffn_set_phase_trace.argtypes = [_P, _P, _I64]
 _lib.pi_hot_first_order.restype = ctypes.c_int
 _lib.pi_hot_first_order.argtypes = [_P, _I32, _P, _P]
 _lib.pi_permute_rows.restype = ctypes.c_int
@@ -155,6 +163,15 @@ def pi_sparse_ffn(h, layer, u, B, idx, count, y, stream=None) -> None:
 def pi_decode_stack(h, x0, B, x_out, counts=None, idx_out=None, stream=None) -> None:
     _check(_lib.pi_decode_stack(h, _ptr(x0), B, _ptr(x_out), _ptr(counts), _ptr(idx_out), _stream(stream)),
            "pi_decode_stack")
+
+
+def pi_decode_stack_layers(h, x0, B, x_out, counts, idx_out, x_layers, stream=None) -> None:
+    _check(_lib.pi_decode_stack_layers(h, _ptr(x0), B, _ptr(x_out), _ptr(counts), _ptr(idx_out), _ptr(x_layers),
+                                       _stream(stream)), "pi_decode_stack_layers")
+
+
+def pi_ffn_set_phase_trace(h, stamps, n_stamps=0) -> None:
+    _check(_lib.pi_ffn_set_phase_trace(h, _ptr(stamps), n_stamps), "pi_ffn_set_phase_trace")
 
 
 def pi_sparse_ffn_noalloc(desc, layer, u, B, idx, count, y, status=None, stream=None) -> None:
@@ -288,6 +305,21 @@ class SparseFFN:
         x_out = torch.empty_like(x0) if x_out is None else x_out
         pi_decode_stack(self.h, x0, x0.shape[0], x_out, counts, idx_out, stream)
         return x_out
+
+    def decode_stack_layers(self, x0, counts=None, idx_out=None, stream=None):
+        """(x_out, x_layers): one decode step, and every layer's output (row l = x_{l+1})."""
+        import torch
+
+        B = x0.shape[0]
+        x_out = torch.empty_like(x0)
+        x_layers = torch.empty((self.desc.n_layers, B, self.desc.d), dtype=torch.float32, device=x0.device)
+        pi_decode_stack_layers(self.h, x0, B, x_out, counts, idx_out, x_layers, stream)
+        return x_out, x_layers
+
+    def set_phase_trace(self, stamps) -> None:
+        """Phase stamps of the persistent step into `stamps` (int64 CUDA tensor
+        [n_layers, PI_STACK_PHASES, n_sm]); None turns them off."""
+        pi_ffn_set_phase_trace(self.h, stamps, 0 if stamps is None else stamps.numel())
 
     def set_hot_neurons(self, n_hot: int) -> None:
         pi_ffn_set_hot_neurons(self.h, n_hot)

@@ -45,9 +45,10 @@ GetRangeFn get_range_fn()
     return fn;
 }
 
-// A pointer the kernels may read or write `bytes` bytes at: non-NULL, aligned,
-// device (or managed) memory of device `dev`, and, where the driver can say,
-// inside one allocation.
+}  // namespace
+
+namespace pi {
+
 pi_status_t check_ptr(const void *p, size_t bytes, size_t align, int dev)
 {
     if (!p || ((uintptr_t)p % align) != 0) return PI_ERR_INVALID_ARG;
@@ -68,6 +69,20 @@ pi_status_t check_ptr(const void *p, size_t bytes, size_t align, int dev)
     return PI_OK;
 }
 
+int injected_fault()
+{
+    const char *v = std::getenv("PI_FAULT");
+    if (!v) return FAULT_NONE;
+    if (!std::strcmp(v, "alloc")) return FAULT_ALLOC;
+    if (!std::strcmp(v, "upload")) return FAULT_UPLOAD;
+    if (!std::strcmp(v, "badarg")) return FAULT_BADARG;
+    return FAULT_NONE;
+}
+
+}  // namespace pi
+
+namespace {
+
 pi_status_t check_opt(const void *p, size_t bytes, size_t align, int dev)
 {
     return p ? check_ptr(p, bytes, align, dev) : PI_OK;
@@ -86,7 +101,7 @@ size_t elt_row_bytes(int dt, int64_t n)
 
 pi_status_t validate_desc(const pi_ffn_desc_t *d)
 {
-    if (!d) return PI_ERR_INVALID_ARG;
+    if (!d || injected_fault() == FAULT_BADARG) return PI_ERR_INVALID_ARG;
     if (d->d < 8 || d->d % 8 || d->f < 1 || d->r < 8 || d->r % 8 || d->n_layers < 1 || d->max_batch < 1 ||
         d->max_batch > 256)
         return PI_ERR_INVALID_ARG;
@@ -101,8 +116,13 @@ pi_status_t validate_desc(const pi_ffn_desc_t *d)
     return PI_OK;
 }
 
-// Largest batch tile (1, 2, 4 or 8) whose fp32 vectors of length K fit the budget, capped near B.
-int pick_bt(int B, int K, int cap = 8)
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+namespace pi {
+
+int pick_bt(int B, int K, int cap)
 {
     int fit = (int)(SMEM_VEC_CAP / ((size_t)K * 4));
     int bt = 1;
@@ -110,9 +130,36 @@ int pick_bt(int B, int K, int cap = 8)
     return bt;
 }
 
-size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+pi_status_t check_layer(const pi_ffn_desc_t &D, const pi_layer_weights_t &w, int dev, bool predictor)
+{
+    const size_t wrow = elt_row_bytes(D.wdtype, D.d), prow = elt_row_bytes(D.pdtype, D.d),
+                 p2row = elt_row_bytes(D.pdtype, D.r);
+    const size_t srow = (size_t)(D.d / 128) * 2;
+    const bool gated = D.kind == PI_FFN_GATED_RELU, int4 = D.wdtype == PI_INT4_G128;
+    pi_status_t s;
+    if ((s = check_ptr(w.w_gate, wrow * D.f, 16, dev))) return s;
+    if ((s = check_ptr(w.w_down_t, wrow * D.f, 16, dev))) return s;
+    if (gated) {
+        if ((s = check_ptr(w.w_up, wrow * D.f, 16, dev))) return s;
+    } else if (w.w_up || w.s_up) {
+        return PI_ERR_INVALID_ARG;
+    }
+    if (int4) {
+        if ((s = check_ptr(w.s_gate, srow * D.f, 2, dev))) return s;
+        if ((s = check_ptr(w.s_down, srow * D.f, 2, dev))) return s;
+        if (gated && (s = check_ptr(w.s_up, srow * D.f, 2, dev))) return s;
+    } else if (w.s_gate || w.s_up || w.s_down) {
+        return PI_ERR_INVALID_ARG;
+    }
+    if ((s = check_opt(w.b_gate, (size_t)D.f * 4, 4, dev))) return s;
+    if (!predictor) return PI_OK;
+    if ((s = check_ptr(w.p1_t, prow * D.r, 16, dev))) return s;
+    if ((s = check_ptr(w.p2_t, p2row * D.f, 16, dev))) return s;
+    if ((s = check_opt(w.b_pred, (size_t)D.f * 4, 4, dev))) return s;
+    return PI_OK;
+}
 
-}  // namespace
+}  // namespace pi
 
 struct pi_ffn {
     pi_ffn_desc_t desc;
@@ -138,6 +185,7 @@ struct pi_ffn {
     float *stack_sumsq = nullptr;
     int stack_slots = 0, stack_slot_bytes = 0;
     size_t stack_smem = 0;
+    unsigned long long *phase_stamps = nullptr;   // pi_ffn_set_phase_trace (borrowed device buffer)
     int off_ring = 0, off_flags = 0, off_mbar = 0, off_ua = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
     // tensor-core path (batch >= tc_min_b)
     bool tc_ok = false;
@@ -166,35 +214,6 @@ pi_status_t cuda_status(cudaError_t e)
     if (e == cudaSuccess) return PI_OK;
     cudaGetLastError();
     return e == cudaErrorMemoryAllocation ? PI_ERR_OOM : PI_ERR_CUDA;
-}
-
-pi_status_t validate_layer(const pi_ffn_t *h, const pi_layer_weights_t &w)
-{
-    const pi_ffn_desc_t &D = h->desc;
-    const size_t wrow = elt_row_bytes(D.wdtype, D.d), prow = elt_row_bytes(D.pdtype, D.d),
-                 p2row = elt_row_bytes(D.pdtype, D.r);
-    const size_t srow = (size_t)(D.d / 128) * 2;
-    const bool gated = D.kind == PI_FFN_GATED_RELU, int4 = D.wdtype == PI_INT4_G128;
-    pi_status_t s;
-    if ((s = check_ptr(w.w_gate, wrow * D.f, 16, h->dev))) return s;
-    if ((s = check_ptr(w.w_down_t, wrow * D.f, 16, h->dev))) return s;
-    if (gated) {
-        if ((s = check_ptr(w.w_up, wrow * D.f, 16, h->dev))) return s;
-    } else if (w.w_up || w.s_up) {
-        return PI_ERR_INVALID_ARG;
-    }
-    if (int4) {
-        if ((s = check_ptr(w.s_gate, srow * D.f, 2, h->dev))) return s;
-        if ((s = check_ptr(w.s_down, srow * D.f, 2, h->dev))) return s;
-        if (gated && (s = check_ptr(w.s_up, srow * D.f, 2, h->dev))) return s;
-    } else if (w.s_gate || w.s_up || w.s_down) {
-        return PI_ERR_INVALID_ARG;
-    }
-    if ((s = check_opt(w.b_gate, (size_t)D.f * 4, 4, h->dev))) return s;
-    if ((s = check_ptr(w.p1_t, prow * D.r, 16, h->dev))) return s;
-    if ((s = check_ptr(w.p2_t, p2row * D.f, 16, h->dev))) return s;
-    if ((s = check_opt(w.b_pred, (size_t)D.f * 4, 4, h->dev))) return s;
-    return PI_OK;
 }
 
 Launch mk(const pi_ffn_t *h, dim3 grid, size_t smem, cudaStream_t s, bool pdl)
@@ -509,43 +528,61 @@ cudaError_t tc_ffn(const pi_ffn_t *h, int layer, int B, const int32_t *idx, cons
     return tc_launch(h, TC_DOWN, nb, a, s, pdl);
 }
 
+// Layer l's output buffer: x_out for the last layer, else row l of x_layers when it is
+// given, else one of the two ping-pong buffers.
+float *layer_out(const pi_ffn_t *h, int l, int B, float *x_out, float *x_layers)
+{
+    if (l == h->desc.n_layers - 1) return x_out;
+    return x_layers ? x_layers + (size_t)l * B * h->desc.d : h->xbuf[l & 1];
+}
+
+// The last layer's output also into the last row of x_layers (when given).
+cudaError_t copy_last_layer(const pi_ffn_t *h, int B, const float *x_out, float *x_layers, cudaStream_t s)
+{
+    if (!x_layers) return cudaSuccess;
+    const size_t n = (size_t)B * h->desc.d;
+    return cudaMemcpyAsync(x_layers + (size_t)(h->desc.n_layers - 1) * n, x_out, n * 4, cudaMemcpyDeviceToDevice, s);
+}
+
 cudaError_t enqueue_stack_tc(const pi_ffn_t *h, const float *x0, int B, float *x_out, int32_t *counts,
-                             int32_t *idx_out, cudaStream_t s)
+                             int32_t *idx_out, float *x_layers, cudaStream_t s)
 {
     const pi_ffn_desc_t &D = h->desc;
     cudaError_t e;
+    const float *xl = x0;
     for (int l = 0; l < D.n_layers; ++l) {
-        const float *xl = l == 0 ? x0 : h->xbuf[(l - 1) & 1];
-        float *xn = l == D.n_layers - 1 ? x_out : h->xbuf[l & 1];
+        float *xn = layer_out(h, l, B, x_out, x_layers);
         int32_t *idx = idx_out ? idx_out + (size_t)l * D.f : h->idx_ws;
         int32_t *cnt = counts ? counts + l : h->counts_ws + l;
         if ((e = tc_split(h, xl, B, 1, s, l > 0)) != cudaSuccess) return e;
         if ((e = tc_predict(h, l, B, idx, cnt, s)) != cudaSuccess) return e;
         if ((e = tc_ffn(h, l, B, idx, cnt, xl, xn, s)) != cudaSuccess) return e;
+        xl = xn;
     }
-    return cudaSuccess;
+    return copy_last_layer(h, B, x_out, x_layers, s);
 }
 
 cudaError_t enqueue_stack(const pi_ffn_t *h, const float *x0, int B, float *x_out, int32_t *counts,
-                          int32_t *idx_out, cudaStream_t s)
+                          int32_t *idx_out, float *x_layers, cudaStream_t s)
 {
     const pi_ffn_desc_t &D = h->desc;
-    if (tc_use(h, B)) return enqueue_stack_tc(h, x0, B, x_out, counts, idx_out, s);
+    if (tc_use(h, B)) return enqueue_stack_tc(h, x0, B, x_out, counts, idx_out, x_layers, s);
     cudaError_t e;
     {
         ProfScope p(h, s, PI_K_RMS);
         e = launch_rms(mk(h, dim3(B), 0, s, false), x0, D.d, B, h->inv_rms, RMS_EPS);
     }
     if (e != cudaSuccess) return e;
+    const float *xl = x0;
     for (int l = 0; l < D.n_layers; ++l) {
-        const float *xl = l == 0 ? x0 : h->xbuf[(l - 1) & 1];
-        float *xn = l == D.n_layers - 1 ? x_out : h->xbuf[l & 1];
+        float *xn = layer_out(h, l, B, x_out, x_layers);
         int32_t *idx = idx_out ? idx_out + (size_t)l * D.f : h->idx_ws;
         int32_t *cnt = counts ? counts + l : h->counts_ws + l;
         if ((e = enqueue_predict(h, l, xl, h->inv_rms, B, idx, cnt, s, true)) != cudaSuccess) return e;
         if ((e = enqueue_ffn(h, l, xl, h->inv_rms, B, idx, cnt, xl, xn, s, true)) != cudaSuccess) return e;
+        xl = xn;
     }
-    return cudaSuccess;
+    return copy_last_layer(h, B, x_out, x_layers, s);
 }
 
 bool legacy_stream(cudaStream_t s) { return s == nullptr || s == cudaStreamLegacy; }
@@ -620,7 +657,7 @@ void plan_stack(pi_ffn_t *h)
 }
 
 cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32_t *counts, int32_t *idx_out,
-                         cudaStream_t st)
+                         float *x_layers, cudaStream_t st)
 {
     const pi_ffn_desc_t &D = h->desc;
     StackArgs a;
@@ -659,6 +696,8 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.hot_k = h->n_hot > 0 ? std::min((h->n_hot + h->nsm - 1) / h->nsm, h->stack_slots - 2) : 0;
     if (a.hot_k < 0) a.hot_k = 0;
     a.p2_stage = a.hot_k > 0 ? 0 : h->stack_p2;   // the hot slots hold the ring between layers
+    a.x_layers = x_layers;
+    a.stamps = h->phase_stamps;
     a.bias_bulk = D.f % 4 == 0 ? 1 : 0;
     for (const pi_layer_weights_t &w : h->layers)
         if (!w.b_gate) a.bias_bulk = 0;
@@ -709,7 +748,7 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
         return s;
     }
     for (int l = 0; l < desc->n_layers; ++l) {
-        if ((s = validate_layer(h, h->layers[l])) != PI_OK) {
+        if ((s = check_layer(h->desc, h->layers[l], h->dev, true)) != PI_OK) {
             delete h;
             return s;
         }
@@ -748,7 +787,8 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
         off[i] = total;
         total = align_up(total + sizes[i], 256);
     }
-    if ((s = cuda_status(cudaMalloc(&h->ws, total))) != PI_OK) {
+    const int fault = injected_fault();
+    if ((s = cuda_status(fault == FAULT_ALLOC ? cudaErrorMemoryAllocation : cudaMalloc(&h->ws, total))) != PI_OK) {
         delete h;
         return s;
     }
@@ -791,8 +831,10 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
             sl[l] = StackLayer{w.w_gate, w.w_up, w.w_down_t, w.s_gate, w.s_up, w.s_down, w.b_gate, w.p1_t, w.p2_t,
                                w.b_pred};
         }
-        if ((s = cuda_status(cudaMemcpy(h->stack_layers, sl.data(), sl.size() * sizeof(StackLayer),
-                                        cudaMemcpyHostToDevice))) != PI_OK) {
+        if ((s = cuda_status(fault == FAULT_UPLOAD ? cudaErrorInvalidValue
+                                                   : cudaMemcpy(h->stack_layers, sl.data(),
+                                                                sl.size() * sizeof(StackLayer),
+                                                                cudaMemcpyHostToDevice))) != PI_OK) {
             cudaFree(h->ws);
             delete h;
             return s;
@@ -849,8 +891,12 @@ pi_status_t pi_sparse_ffn(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
     return cuda_status(enqueue_ffn(h, layer, u, nullptr, B, idx, count, nullptr, y, (cudaStream_t)stream, false));
 }
 
-pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_out, int32_t *counts,
-                            int32_t *idx_out, void *stream)
+}  // extern "C"
+
+namespace {
+
+pi_status_t decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_out, int32_t *counts, int32_t *idx_out,
+                         float *x_layers, void *stream)
 {
     if (!h || B < 1 || B > h->desc.max_batch) return PI_ERR_INVALID_ARG;
     const pi_ffn_desc_t &D = h->desc;
@@ -859,11 +905,12 @@ pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_ou
     if ((s = check_ptr(x_out, (size_t)B * D.d * 4, 16, h->dev))) return s;
     if ((s = check_opt(counts, (size_t)D.n_layers * 4, 4, h->dev))) return s;
     if ((s = check_opt(idx_out, (size_t)D.n_layers * D.f * 4, 4, h->dev))) return s;
+    if ((s = check_opt(x_layers, (size_t)D.n_layers * B * D.d * 4, 16, h->dev))) return s;
     cudaStream_t st = (cudaStream_t)stream;
 
     if (B == 1 && h->stack_ok) {
         ProfScope p(h, st, PI_K_STACK);
-        cudaError_t e = launch_stack(h, x0, x_out, counts, idx_out, st);
+        cudaError_t e = launch_stack(h, x0, x_out, counts, idx_out, x_layers, st);
         if (e == cudaSuccess) return PI_OK;
         cudaGetLastError();
         if (e != cudaErrorNotSupported && e != cudaErrorCooperativeLaunchTooLarge) return cuda_status(e);
@@ -872,8 +919,8 @@ pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_ou
 
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (!legacy_stream(st) && cudaStreamIsCapturing(st, &cs) != cudaSuccess) return cuda_status(cudaGetLastError());
-    if (legacy_stream(st) || cs != cudaStreamCaptureStatusNone || h->prof)
-        return cuda_status(enqueue_stack(h, x0, B, x_out, counts, idx_out, st));
+    if (legacy_stream(st) || cs != cudaStreamCaptureStatusNone || h->prof || x_layers)
+        return cuda_status(enqueue_stack(h, x0, B, x_out, counts, idx_out, x_layers, st));
 
     if (!(h->gexec && h->g_B == B && h->g_x0 == x0 && h->g_xout == x_out && h->g_counts == counts &&
           h->g_idx == idx_out)) {
@@ -883,7 +930,7 @@ pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_ou
         }
         cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeRelaxed);
         if (e != cudaSuccess) return cuda_status(e);
-        cudaError_t el = enqueue_stack(h, x0, B, x_out, counts, idx_out, st);
+        cudaError_t el = enqueue_stack(h, x0, B, x_out, counts, idx_out, nullptr, st);
         cudaGraph_t g = nullptr;
         e = cudaStreamEndCapture(st, &g);
         if (el != cudaSuccess || e != cudaSuccess) {
@@ -903,6 +950,38 @@ pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_ou
         h->g_idx = idx_out;
     }
     return cuda_status(cudaGraphLaunch(h->gexec, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_out, int32_t *counts,
+                            int32_t *idx_out, void *stream)
+{
+    return decode_stack(h, x0, B, x_out, counts, idx_out, nullptr, stream);
+}
+
+pi_status_t pi_decode_stack_layers(pi_ffn_t *h, const float *x0, int32_t B, float *x_out, int32_t *counts,
+                                   int32_t *idx_out, float *x_layers, void *stream)
+{
+    if (!x_layers) return PI_ERR_INVALID_ARG;
+    return decode_stack(h, x0, B, x_out, counts, idx_out, x_layers, stream);
+}
+
+pi_status_t pi_ffn_set_phase_trace(pi_ffn_t *h, uint64_t *stamps, int64_t n_stamps)
+{
+    if (!h) return PI_ERR_INVALID_ARG;
+    if (!stamps) {
+        h->phase_stamps = nullptr;
+        return PI_OK;
+    }
+    const int64_t need = (int64_t)h->desc.n_layers * STACK_PHASES * h->nsm;
+    if (n_stamps < need) return PI_ERR_INVALID_ARG;
+    pi_status_t s;
+    if ((s = check_ptr(stamps, (size_t)need * 8, 8, h->dev))) return s;
+    h->phase_stamps = reinterpret_cast<unsigned long long *>(stamps);
+    return PI_OK;
 }
 
 pi_status_t pi_ffn_set_hot_prefix(pi_ffn_t *h, int32_t n_hot)

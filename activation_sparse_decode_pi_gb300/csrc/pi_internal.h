@@ -6,7 +6,29 @@
 
 #include <unordered_map>
 
+#include "pi_ffn.h"
+
 namespace pi {
+
+// ---------------------------------------------------------------- host-side validation (pi_api.cu)
+
+// A pointer the kernels may read or write `bytes` bytes at: non-NULL, aligned, device (or
+// managed) memory of device `dev`, and, where the driver can say, inside one allocation.
+pi_status_t check_ptr(const void *p, size_t bytes, size_t align, int dev);
+
+// Every weight pointer of one layer for its shape: sizes inside their allocations, 16-byte
+// aligned rows, NULL exactly where the kind and type say. predictor: also p1_t / p2_t / b_pred.
+pi_status_t check_layer(const pi_ffn_desc_t &D, const pi_layer_weights_t &w, int dev, bool predictor);
+
+// Largest batch tile (1, 2, 4 or 8, at most cap) whose fp32 vectors of length K fit the
+// shared-memory budget of one staged tile, capped near B.
+int pick_bt(int B, int K, int cap = 8);
+
+// Host-side fault injection, read from PI_FAULT at each pi_ffn_create: "alloc" fails the
+// workspace allocation (nothing is allocated), "upload" fails after the workspace exists
+// (the clean-up path frees it), "badarg" fails descriptor validation.
+enum { FAULT_NONE = 0, FAULT_ALLOC = 1, FAULT_UPLOAD = 2, FAULT_BADARG = 3 };
+int injected_fault();
 
 // Launch geometry shared by host and kernels.
 constexpr int NT = 256;               // threads per CTA of the CUDA-core kernels
@@ -63,7 +85,12 @@ struct StackArgs {
     int hot_k;                    // ring slots per CTA held by hot owned neurons (loaded a layer ahead), <= slots - 2
     int hot_prefix;               // neurons below this are active without a logit
     int p2_stage;                 // owned P2 rows per CTA copied into the ring ahead of their layer (0: none)
+    float *x_layers;              // optional [L x d]: row l = x_{l+1} (every layer's output), or NULL
+    unsigned long long *stamps;   // optional [L x STACK_PHASES x grid] %globaltimer stamps, or NULL
 };
+
+// Phase boundaries the persistent step can stamp per layer and CTA (pi_ffn_set_phase_trace).
+constexpr int STACK_PHASES = 8;
 
 template <int WT>
 cudaError_t launch_stack_wt(int pdt, int kind, const StackArgs &a, int grid, size_t smem, cudaStream_t s);

@@ -20,6 +20,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "pi_ffn.h"
 #include "pi_internal.h"
@@ -31,36 +32,64 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PI_NOALLOC_SCRA
 namespace {
 
 constexpr int MAX_DEVICES = 64;
-void *g_scratch_ptr[MAX_DEVICES] = {};
 
-// Device address of the scratch array on the current device. Host code cannot
-// use the array's name as a device address; it asks the runtime once per device.
+// The array's device address, looked up once per device and context. Host code cannot use the
+// array's name as a device address (it names a host-side stand-in), so the runtime is asked,
+// with the device current. The entry is refreshed when the device's context changes (after a
+// cudaDeviceReset the module is loaded again, possibly elsewhere). A mutex makes concurrent
+// first calls from several host threads safe.
+struct ScratchSlot {
+    unsigned long long ctx = 0;   // context id the address belongs to (0: unknown)
+    void *ptr = nullptr;
+};
+ScratchSlot g_slots[MAX_DEVICES];
+std::mutex g_slots_mu;
+
+typedef CUresult (*CtxCurrentFn)(CUcontext *);
+typedef CUresult (*CtxIdFn)(CUcontext, unsigned long long *);
+
+void *driver_entry(const char *name)
+{
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return p;
+}
+
+// Unique id of the calling thread's current context, 0 if the driver cannot say.
+unsigned long long current_ctx_id()
+{
+    static CtxCurrentFn get_cur = (CtxCurrentFn)driver_entry("cuCtxGetCurrent");
+    static CtxIdFn get_id = (CtxIdFn)driver_entry("cuCtxGetId");
+    if (!get_cur || !get_id) return 0;
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_cur(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 pi_status_t scratch_for(int dev, void **out)
 {
     if (dev < 0 || dev >= MAX_DEVICES) return PI_ERR_UNSUPPORTED;
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) {
-            cudaGetLastError();
-            return PI_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
+    std::lock_guard<std::mutex> lock(g_slots_mu);
+    ScratchSlot &slot = g_slots[dev];
+    const unsigned long long id = current_ctx_id();
+    if (slot.ptr && id != 0 && slot.ctx == id) {
+        *out = slot.ptr;
+        return PI_OK;
     }
-    *out = g_scratch_ptr[dev];
-    return PI_OK;
-}
-
-pi_status_t check_dev_ptr(const void *p, size_t align, int dev)
-{
-    if (!p || ((uintptr_t)p % align) != 0) return PI_ERR_INVALID_ARG;
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
         cudaGetLastError();
-        return PI_ERR_INVALID_ARG;
+        return PI_ERR_CUDA;
     }
-    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return PI_ERR_INVALID_ARG;
-    if (a.type == cudaMemoryTypeDevice && a.device != dev) return PI_ERR_INVALID_ARG;
+    slot.ptr = p;
+    slot.ctx = current_ctx_id();   // the lookup above created the context if there was none
+    *out = p;
     return PI_OK;
 }
 
@@ -91,18 +120,13 @@ extern "C" pi_status_t pi_sparse_ffn_noalloc(const pi_ffn_desc_t *desc, const pi
         return PI_ERR_CUDA;
     }
     pi_status_t s;
-    const bool gated = D.kind == PI_FFN_GATED_RELU, int4 = D.wdtype == PI_INT4_G128;
-    if ((s = check_dev_ptr(layer->w_gate, 16, dev))) return s;
-    if ((s = check_dev_ptr(layer->w_down_t, 16, dev))) return s;
-    if (gated && (s = check_dev_ptr(layer->w_up, 16, dev))) return s;
-    if (int4 && ((s = check_dev_ptr(layer->s_gate, 2, dev)) || (s = check_dev_ptr(layer->s_down, 2, dev)) ||
-                 (gated && (s = check_dev_ptr(layer->s_up, 2, dev)))))
-        return s;
-    if (layer->b_gate && (s = check_dev_ptr(layer->b_gate, 4, dev))) return s;
-    if ((s = check_dev_ptr(u, 16, dev)) || (s = check_dev_ptr(idx, 4, dev)) || (s = check_dev_ptr(count, 4, dev)) ||
-        (s = check_dev_ptr(y, 16, dev)))
-        return s;
-    if (status && (s = check_dev_ptr(status, 4, dev))) return s;
+    const bool int4 = D.wdtype == PI_INT4_G128;
+    // the same checks as a handle's: every byte the kernels touch lies inside its allocation
+    if ((s = check_layer(D, *layer, dev, false))) return s;
+    const size_t vec = (size_t)B * D.d * 4;
+    if ((s = check_ptr(u, vec, 16, dev)) || (s = check_ptr(y, vec, 16, dev))) return s;
+    if ((s = check_ptr(idx, 4, 4, dev)) || (s = check_ptr(count, 4, 4, dev))) return s;   // idx: *count entries, checked on the device
+    if (status && (s = check_ptr(status, 4, 4, dev))) return s;
 
     void *scratch = nullptr;
     if ((s = scratch_for(dev, &scratch))) return s;
@@ -120,10 +144,7 @@ extern "C" pi_status_t pi_sparse_ffn_noalloc(const pi_ffn_desc_t *desc, const pi
         L.nsm = nsm;
         return L;
     };
-    int bt = 1;
-    while (bt * 2 <= 8 && (size_t)bt * 2 * D.d * 4 <= SMEM_VEC_CAP && bt < B) bt *= 2;
-    int btd = 1;
-    while (btd * 2 <= (int4 ? 2 : 8) && btd < B) btd *= 2;
+    const int bt = pick_bt(B, D.d), btd = pick_bt(B, 1, int4 ? 2 : 8);   // the tiles pi_sparse_ffn picks
     uint32_t *st_word = (uint32_t *)status;
     cudaError_t e = launch_ffn_h(mk(dim3(0), (size_t)bt * D.d * 4, false), D.wdtype, D.kind, bt, layer->w_gate,
                                  layer->w_up, layer->s_gate, layer->s_up, layer->b_gate, D.d, D.f, u, nullptr, B, idx,

@@ -249,6 +249,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     // slot HK + n % SC with parity (n / SC) & 1.
     uint32_t cseq = 0;
     unsigned kb = 0;    // grid barriers passed in this launch
+    // optional %globaltimer stamp of phase boundary ph of layer l (thread 0 of each CTA)
+    auto stamp = [&](int l, int ph) {
+        if (a.stamps && tid == 0) a.stamps[((size_t)l * STACK_PHASES + ph) * P + c] = globaltimer_ns();
+    };
     auto sync_grid = [&](auto work) -> bool {
         ++kb;
         const PendingCopies pc{&s_p2bar, mbar, min(a.hot_k, K), s_pend};
@@ -335,6 +339,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
         const float *xl = l == 0 ? a.x0 : (((l - 1) & 1) ? a.xb : a.xa);
         float *xn = l == a.L - 1 ? a.x_out : ((l & 1) ? a.xb : a.xa);
         float inv;   // RMS scale of x_l
+        stamp(l, 0);
 
         // ------------------------------------------------------------ A: predictor hidden layer
         {
@@ -401,7 +406,9 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             }
             cp_async_wait_all();
         }
+        stamp(l, 1);
         if (!sync_grid(no_work)) return;
+        stamp(l, 2);
 
         // ------------------------------------------------------------ BC: logits, then the sparse FFN
         {
@@ -562,6 +569,8 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             }
             if (tid == 0 && a.counts && nn) atomicAdd(a.counts + l, nn);
             __syncthreads();
+            stamp(l, 3);
+            if (nn == 0) stamp(l, 4);
 
             // list entries [0, nh) are hot (already in their slots), [nh, nn) cold
             const int HK = a.hot_k, SC = S - HK, hk = min(HK, K);
@@ -696,6 +705,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     }
                     return;
                 }
+                if (bi == 0) stamp(l, 4);
                 // the previous cold batch's slots are free: entry k + SC takes entry k's slot
                 // (copy j of the batch's w-th refill goes to the thread that took copy j of cold entry w)
                 if (cold && m0 - nbc >= nh && cw < nbc && m0 - nbc + cw + SC < nn) {
@@ -759,6 +769,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     reinterpret_cast<float4 *>(pq + (size_t)ci * VW)[e4] =
                         make_float4(yr[cc][4 * e4], yr[cc][4 * e4 + 1], yr[cc][4 * e4 + 2], yr[cc][4 * e4 + 3]);
             }
+            stamp(l, 5);
         }
         // Once every thread is done with the ring (the barrier's CTA sync), the next layer's hot
         // rows (a whole layer before their predictor runs) or its staged P2 rows are requested
@@ -775,6 +786,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 if (l + 1 < a.L && KS > 0) stage_p2(s_p2next);
             }))
             return;
+        stamp(l, 6);
 
         // ------------------------------------------------------------ D: fixed-order reduction + residual
         {
@@ -803,6 +815,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                         const float4 xv = __ldcg(reinterpret_cast<const float4 *>(xl + col));
                         y.x += xv.x; y.y += xv.y; y.z += xv.z; y.w += xv.w;
                         *reinterpret_cast<float4 *>(xn + col) = y;
+                        if (a.x_layers) *reinterpret_cast<float4 *>(a.x_layers + (size_t)l * d + col) = y;
                         ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
                     }
                     ss += __shfl_xor_sync(0xffu, ss, 1);
@@ -833,6 +846,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 }
                 __syncthreads();
             }
+            stamp(l, 7);
             if (l + 1 < a.L && !sync_grid(no_work)) return;
         }
     }

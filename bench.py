@@ -2,18 +2,23 @@
 
 One step = one decode token (one per sequence of the batch) through every layer of
 the stack via pi_decode_stack: predictor -> union mask -> gate/up gather -> W_down
-axpy -> deterministic reduce, per layer. Default workload: ReluLLaMA-7B-shaped stack
-(32 gated-ReLU FFN layers, d=4096, f=11008, bf16, predictor rank 1024), batch 1,
-synthetic seeded weights and inputs. Each step streams ~1.9 GB of distinct weights,
-far more than the 129 MB L2, so steps run with inputs larger than L2 (no flush needed).
+axpy -> deterministic reduce, per layer. Default workload: the largest batch-1 stack,
+OPT-175B-shaped (96 non-gated ReLU FFN layers, d=12288, f=49152, int4 group-128
+weights with fp16 scales, fp16 predictor of rank 1024), batch 1, synthetic seeded
+weights and inputs. Each step streams ~14.5 GB of distinct weights, far more than the
+129 MB L2, so steps run with inputs larger than L2 (no flush needed).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--batch B] [--layers L] [--rank R]
                   [--hot-prefix-fraction F] [--hot-fraction G] [--no-cpu-baseline]
+                  [--phase-trace]
 
 --impl reference times the CPU fp64 oracle on the host cores, on a bounded sample
-of the same workload. --rank runs the predictor-rank sweep's variants, and
---hot-prefix-fraction the hot-prefix variant of the method. Under torchrun (N > 1)
+of the same workload (the first layers of the stack; every layer has the same shape
+and activation law, so the time per token is scaled to all layers). --phase-trace adds
+the persistent batch-1 kernel's per-layer phase times (a separate, untimed run).
+--rank runs the predictor-rank sweep's variants, and --hot-prefix-fraction the
+hot-prefix variant of the method. Under torchrun (N > 1)
 every rank decodes its own token stream with the same weights (independent
 sequences, weak scaling, no data-path collective); only a barrier and a max over
 ranks of the timed region are exchanged.
@@ -37,7 +42,7 @@ sys.path.insert(0, ROOT)
 
 from workload import WORKLOADS, make_inputs, make_layer  # noqa: E402
 
-DEFAULT_WORKLOAD = "relullama7b_d4096_f11008_bf16_L32"
+DEFAULT_WORKLOAD = "opt175b_d12288_f49152_int4_L96"
 CSRC = os.path.join(ROOT, "activation_sparse_decode_pi_gb300", "csrc")
 
 # DRAM traffic of the dominant kernel per launch, from one ncu capture (dram__bytes_read.sum +
@@ -259,31 +264,107 @@ def build_model(w, device):
     return layers, counts
 
 
-def cpu_baseline(w, B, seconds: float = 15.0, max_tokens: int = 64):
-    """The oracle, as it stands, on the host cores: tokens/s over a bounded sample."""
+def oracle_layer(w, l, device):
+    """Layer l as the oracle's numpy arrays, put in hot-first order with the oracle's own order."""
     import oracle
 
+    L = make_layer(w, l, 0, device=device)
+    perm = oracle.hot_first_order(L["counts"].cpu().numpy())
+    Lo = oracle.layer_numpy(L)
+    for k in ("w_gate", "w_up", "w_down_t", "s_gate", "s_up", "s_down", "b_gate", "p2_t", "b_pred"):
+        if Lo.get(k) is not None:
+            Lo[k] = np.ascontiguousarray(Lo[k][perm])
+    del L
+    return Lo
+
+
+HOST_SAMPLE_BYTES = 6e9   # host memory the oracle's layer sample may take
+
+
+def sample_layers(w) -> int:
+    """Layers of the oracle's bounded sample: the first ones, as many as fit HOST_SAMPLE_BYTES."""
+    per_layer = (w.f * neuron_bytes(w) + predictor_bytes(w))
+    return int(max(1, min(w.n_layers, HOST_SAMPLE_BYTES // per_layer)))
+
+
+def oracle_token(x, layers, w):
+    """One decode token through `layers` with the oracle, as it stands (oracle.stack)."""
+    import oracle
+
+    return oracle.stack(x.astype(np.float64), layers, w.kind, w.wdtype, w.pdtype)["x_out"]
+
+
+def cpu_baseline(w, B, seconds: float = 15.0, max_tokens: int = 64):
+    """The oracle, as it stands, on the host cores: tokens/s over a bounded sample (the first
+    M layers of the stack, scaled to all of them: every layer has the same shape and law)."""
+    import oracle
+
+    M = sample_layers(w)
     x = make_inputs(w, POOL_TOKENS, B, 0, device="cpu").numpy()
-    layers = []
-    for l in range(w.n_layers):
-        L = make_layer(w, l, 0, device="cuda")
-        perm = oracle.hot_first_order(L["counts"].cpu().numpy())
-        Lo = oracle.layer_numpy(L)
-        for k in ("w_gate", "w_up", "w_down_t", "s_gate", "s_up", "s_down", "b_gate", "p2_t", "b_pred"):
-            if Lo.get(k) is not None:
-                Lo[k] = np.ascontiguousarray(Lo[k][perm])
-        layers.append(Lo)
-        del L
+    layers = [oracle_layer(w, l, "cuda") for l in range(M)]
     torch.cuda.empty_cache()
     t0 = time.perf_counter()
     n = 0
     while n < max_tokens and (time.perf_counter() - t0) < seconds:
-        oracle.stack(x[n].astype(np.float64), layers, w.kind, w.wdtype, w.pdtype)
+        oracle_token(x[n], layers, w)
         n += 1
     dt = time.perf_counter() - t0
-    return {"value": n * B / dt, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{n} decode steps x batch {B} through all {w.n_layers} layers of {w.name} "
-                      f"(fp64 C oracle, OpenMP), {dt:.1f} s"}
+    per_token = dt / n * w.n_layers / M
+    return {"value": B / per_token, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{n} decode steps x batch {B} through the first {M} of the {w.n_layers} layers of {w.name} "
+                      f"(fp64 C oracle, OpenMP), {dt:.1f} s, time per token scaled by {w.n_layers}/{M}"}
+
+
+def config_of(w, B, world, hot_neurons=0, hot_prefix=0):
+    """The workload as the JSON line names it (both arms)."""
+    return {"workload": w.name, "d": w.d, "f": w.f, "r": w.r, "layers": w.n_layers, "kind": w.kind,
+            "weights": w.wdtype, "predictor": w.pdtype, "batch": B, "global_batch": B * world,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": (f"inputs larger than L2: every step streams {predictor_bytes(w) * w.n_layers / 1e9:.2f} GB of "
+                   "predictor weights plus the active rows (L2 is 129 MB)")
+            if predictor_bytes(w) * w.n_layers > 129e6 else "L2-resident stack (no HBM claim)",
+            "hot_neurons": hot_neurons, "hot_prefix": hot_prefix}
+
+
+def phase_trace(P, ffn, step, w, n_steps: int):
+    """Per-layer phase times of the persistent batch-1 kernel (microseconds): for each phase, the
+    median over layers and steps of the mean and of the max over CTAs. A separate, untimed run."""
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    stamps = torch.zeros((w.n_layers, P.PI_STACK_PHASES, nsm), dtype=torch.int64, device="cuda")
+    ffn.set_phase_trace(stamps)
+    rows = []
+    try:
+        for i in range(n_steps + 2):
+            step(i)
+            torch.cuda.synchronize()
+            if i >= 2:   # the first steps warm the trace path
+                rows.append(stamps.cpu().numpy().astype(np.float64))
+    finally:
+        ffn.set_phase_trace(None)
+    if not rows:
+        return None
+    names = ["hidden", "barrier_1", "logits_list", "first_rows", "ffn_rest", "barrier_2", "reduce", "barrier_3"]
+    acc = {n: ([], []) for n in names}
+    layer_us = []
+    for st in rows:
+        for l in range(w.n_layers):
+            s0 = st[l]
+            nxt = st[l + 1][0] if l + 1 < w.n_layers else None
+            seg = [s0[1] - s0[0], s0[2] - s0[1], s0[3] - s0[2], s0[4] - s0[3], s0[5] - s0[4], s0[6] - s0[5],
+                   s0[7] - s0[6], (nxt - s0[7]) if nxt is not None else None]
+            for n, v in zip(names, seg):
+                if v is None:
+                    continue
+                acc[n][0].append(float(np.mean(v)) / 1e3)
+                acc[n][1].append(float(np.max(v)) / 1e3)
+            if nxt is not None:
+                layer_us.append(float(np.min(nxt) - np.min(s0[0])) / 1e3)
+    out = {n: {"mean_us": statistics.median(a), "max_us": statistics.median(b)} for n, (a, b) in acc.items() if a}
+    out["layer_us"] = statistics.median(layer_us) if layer_us else None
+    out["steps"] = len(rows)
+    out["how"] = ("%globaltimer stamps of thread 0 of every CTA at each phase boundary (pi_ffn_set_phase_trace); "
+                  "per phase: median over layers and steps of the mean / max over CTAs")
+    return out
 
 
 def workload_of(args):
@@ -381,30 +462,34 @@ def run_ours(args):
                         "gbs": kernel_bytes(w, k, mean_count, B, mean_counts, hot_prefix) / (v[0] / v[1] / 1e3) / 1e9}
                     for k, v in kinds.items()}
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region.
+    # Decode is sequential: token t's output is on the host before token t+1's input is sent.
     Xh = X.cpu().pin_memory()
     out_h = torch.empty((B, w.d), dtype=torch.float32).pin_memory()
     e2e_steps = args.steps
+    done = torch.cuda.Event()
 
     def e2e_step(i):
         with torch.cuda.stream(s):
             x_in.copy_(Xh[i % POOL_TOKENS], non_blocking=True)
             P.pi_decode_stack(ffn.h, x_in, B, x_out, counts, None, s)
             out_h.copy_(x_out, non_blocking=True)
+            done.record(s)
+        done.synchronize()
 
     for i in range(args.warmup):
         e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
-    e0.record(s)
+    h0 = time.perf_counter()
     for i in range(e2e_steps):
         e2e_step(i)
-    e1.record(s)
     torch.cuda.synchronize()
-    e2e_ms, e2e_tokens = aggregate(e0.elapsed_time(e1), e2e_steps * B, world)
+    e2e_ms, e2e_tokens = aggregate((time.perf_counter() - h0) * 1e3, e2e_steps * B, world)
     barrier(world)
 
     launches_per_step = sum(v[1] for v in kinds.values()) / prof_steps   # our kernels per decode step
+    phases = phase_trace(P, ffn, step, w, args.phase_trace_steps) if args.phase_trace and B == 1 else None
     line = {
         "metric": METRIC,
         "value": tokens / (ms / 1e3),
@@ -418,11 +503,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": w.wdtype,
         "data": "synthetic (seeded weights with the workload's shapes and Zipf activation statistics; x ~ N(0,1))",
-        "config": {"workload": w.name, "d": w.d, "f": w.f, "r": w.r, "layers": w.n_layers, "kind": w.kind,
-                   "weights": w.wdtype, "predictor": w.pdtype, "batch": B, "global_batch": B * world,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"inputs larger than L2: {bytes_per_step / 1e9:.2f} GB of distinct weights per step",
-                   "hot_neurons": n_hot, "hot_prefix": hot_prefix},
+        "config": config_of(w, B, world, n_hot, hot_prefix),
         "hbm_gbs": hbm_gbs,
         "hbm_frac": hbm_gbs / peak,
         "bytes_per_step": bytes_per_step,
@@ -437,9 +518,12 @@ def run_ours(args):
         "kernels": kernel_table,
         "clocks": clocks,
         "e2e": {"value": e2e_tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": B * w.d * 4,
-                "d2h_bytes_per_step": B * w.d * 4},
+                "d2h_bytes_per_step": B * w.d * 4,
+                "note": "host clock; each step waits for its output on the host before the next input is sent"},
         "gpu_launches": int(round(args.steps * launches_per_step)),
     }
+    if phases is not None:
+        line["phases"] = phases
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         del layers, ffn
         torch.cuda.empty_cache()
@@ -465,32 +549,26 @@ def run_reference(args):
     w = workload_of(args)
     B = args.batch
     gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    M = sample_layers(w)
     x = make_inputs(w, POOL_TOKENS, B, 1000, device="cpu").numpy()
-    layers = []
-    for l in range(w.n_layers):
-        L = make_layer(w, l, 0, device=gen_dev)
-        perm = oracle.hot_first_order(L["counts"].cpu().numpy())
-        Lo = oracle.layer_numpy(L)
-        for k in ("w_gate", "w_up", "w_down_t", "s_gate", "s_up", "s_down", "b_gate", "p2_t", "b_pred"):
-            if Lo.get(k) is not None:
-                Lo[k] = np.ascontiguousarray(Lo[k][perm])
-        layers.append(Lo)
+    layers = [oracle_layer(w, l, gen_dev) for l in range(M)]
     for i in range(args.warmup):
-        oracle.stack(x[i % POOL_TOKENS].astype(np.float64), layers, w.kind, w.wdtype, w.pdtype)
+        oracle_token(x[i % POOL_TOKENS], layers, w)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle.stack(x[(args.warmup + i) % POOL_TOKENS].astype(np.float64), layers, w.kind, w.wdtype, w.pdtype)
-    dt = time.perf_counter() - t0
+        oracle_token(x[(args.warmup + i) % POOL_TOKENS], layers, w)
+    dt = (time.perf_counter() - t0) * w.n_layers / M     # scaled to all layers
     v = args.steps * B / dt
+    sample = (f"{args.steps} timed decode steps x batch {B} (after {args.warmup} warm-up) through the first {M} "
+              f"of the {w.n_layers} layers, time per token scaled by {w.n_layers}/{M}")
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (same seeded workload as the GPU arm)",
-        "config": {"workload": w.name, "d": w.d, "f": w.f, "r": w.r, "layers": w.n_layers, "batch": B},
+        "config": config_of(w, B, world),
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
-                         "sample": f"{args.steps} timed decode steps x batch {B} (after {args.warmup} warm-up) "
-                                   f"through all {w.n_layers} layers"},
+                         "sample": sample},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -507,6 +585,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=None,
                     help="use only the first L layers (small-footprint profiling runs; default: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--phase-trace", action="store_true",
+                    help="add the persistent batch-1 kernel's per-layer phase times (separate untimed run)")
+    ap.add_argument("--phase-trace-steps", type=int, default=8)
     ap.add_argument("--hot-prefix-fraction", type=float, default=0.0,
                     help="the hot-prefix variant: neurons that fired on at least this fraction of the profiling "
                          "tokens are computed on every token, the predictor decides the rest; 0 (default) is the "

@@ -42,6 +42,10 @@
  *    2), ring depth cap, and CTAs per predictor-hidden tile (default 8).
  * They change speed and, for some, the order of floating-point additions (so the output
  * bits), not what is computed.
+ *  - PI_FAULT=alloc|upload|badarg  host-side fault injection for failure-path tests:
+ *    pi_ffn_create then fails its workspace allocation (PI_ERR_OOM, nothing allocated),
+ *    fails after the workspace exists (PI_ERR_CUDA, the workspace is freed again), or
+ *    rejects the descriptor (PI_ERR_INVALID_ARG). *out is NULL in every case.
  */
 #ifndef PI_FFN_H
 #define PI_FFN_H
@@ -141,6 +145,9 @@ pi_status_t pi_predict(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
  * bits of y depend only on the inputs. Any index list is accepted (ascending or not,
  * empty when *count == 0); entries outside [0, f) are skipped and flagged.
  * u: [B x d] fp32; idx: [>= *count] int32; count: one int32 (device); y: [B x d] fp32 out.
+ * Argument errors are found before any launch. If the CUDA runtime refuses a later launch of
+ * the chain (not an argument error), PI_ERR_CUDA is returned with the earlier kernels already
+ * enqueued; they write only the workspace, and y is then not written.
  */
 pi_status_t pi_sparse_ffn(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
                           const int32_t *idx, const int32_t *count, float *y, void *stream);
@@ -166,6 +173,34 @@ pi_status_t pi_sparse_ffn(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
  */
 pi_status_t pi_decode_stack(pi_ffn_t *h, const float *x0, int32_t B, float *x_out,
                             int32_t *counts, int32_t *idx_out, void *stream);
+
+/*
+ * pi_decode_stack that also keeps every layer's output, for checking a step layer by layer
+ * (the walk-through page's inference flow hands each layer's merged output to the next
+ * layer; this exposes those hand-offs). Computes exactly what pi_decode_stack computes, on
+ * the same kernels, and writes x_{l+1} to row l of x_layers.
+ * x_layers: [n_layers x B x d] fp32 device, out (row n_layers - 1 equals x_out); not NULL.
+ * The multi-kernel chain then runs without its recorded graph. Other arguments and errors
+ * as pi_decode_stack.
+ */
+pi_status_t pi_decode_stack_layers(pi_ffn_t *h, const float *x0, int32_t B, float *x_out,
+                                   int32_t *counts, int32_t *idx_out, float *x_layers, void *stream);
+
+/*
+ * Phase timing of the persistent batch-1 step (tracing aid; off by default). With a buffer
+ * set, every later pi_decode_stack / pi_decode_stack_layers call that runs the persistent
+ * kernel writes, per layer l, phase boundary p < PI_STACK_PHASES and CTA c (one CTA per SM),
+ * the GPU's nanosecond global timer to stamps[(l * PI_STACK_PHASES + p) * n_sm + c].
+ * Boundaries: 0 layer start (predictor hidden layer), 1 hidden layer done, 2 after the grid
+ * barrier (logits start), 3 active list ready, 4 first batch of active rows landed (= 3 when
+ * the CTA has no active neuron), 5 the CTA's FFN partial written, 6 after the grid barrier
+ * (reduction start), 7 reduction done. Only thread 0 of each CTA writes; one store per
+ * boundary. stamps: device, 8-byte aligned, n_stamps >= n_layers * PI_STACK_PHASES * n_sm
+ * (n_sm = the device's multiprocessor count), borrowed until it is replaced or cleared.
+ * NULL clears it. Returns PI_ERR_INVALID_ARG for a short or non-device buffer.
+ */
+#define PI_STACK_PHASES 8
+pi_status_t pi_ffn_set_phase_trace(pi_ffn_t *h, uint64_t *stamps, int64_t n_stamps);
 
 /*
  * Offline hot-first order (walk-through page, section "offline profiling", code
@@ -220,12 +255,20 @@ pi_status_t pi_profile_end(pi_ffn_t *h, float *ms, int32_t *launches, int32_t n_
  * until process exit. The call needs (B*f rounded up to 64 + 256*B*d) * 4 bytes of it
  * and returns PI_ERR_UNSUPPORTED, launching nothing, when that exceeds the array.
  * Set-up: the first call on each device looks up the array's device address with
- * that device current; make that first call before any stream capture.
+ * that device current (again after the device's context changes, e.g. after a
+ * cudaDeviceReset); make that first call before any stream capture. The lookup is
+ * guarded by a mutex, so first calls from several host threads are safe.
  * Every call shares the array and it keeps the previous call's contents (this path
  * needs none of it zeroed); calls whose kernels overlap on the GPU race on it, so
- * order them on one stream. status: optional int32 device word; a kernel that
+ * order them on one stream. u and y must hold B*d floats, idx and count as for
+ * pi_sparse_ffn; pointers are checked like a handle's (inside their allocations).
+ * status: optional int32 device word; a kernel that
  * rejects a list entry or count sets it to PI_ERR_DEVICE_CHECK if it is 0 (clear it
  * before the call). No cudaMalloc, cudaFree or other allocating call is made.
+ * The three kernels are launched one after another: every argument error is found
+ * before the first launch, but if the CUDA runtime refuses the second or third
+ * launch, the call returns PI_ERR_CUDA with the earlier kernels already enqueued
+ * (they write only the scratch array), and y is not written.
  */
 #define PI_NOALLOC_SCRATCH_BYTES (16u << 20)
 

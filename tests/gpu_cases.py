@@ -59,3 +59,41 @@ def to_dev(a, dtype=None):
     if dtype is not None:
         t = t.to(dtype)
     return t.cuda()
+
+
+def teacher_forced(P, w, layers, ffn, x0, hot_prefix=0, tag=""):
+    """One decode step checked layer by layer, teacher-forced.
+
+    Layer l of the oracle runs on the GPU's own input x_l (pi_decode_stack_layers keeps every
+    layer's output), so every layer is compared, including those after an in-band difference
+    upstream: (1) the GPU's active list equals the oracle's outside the 1e-4 band, and (2)
+    y_l = x_{l+1} - x_l is within the dtype's bar of the oracle's sparse FFN evaluated on the
+    GPU's own list (an in-band difference is then not counted twice).
+    Returns (x_out as numpy, number of layers with an in-band difference).
+    """
+    x0 = np.asarray(x0, np.float32)
+    B = x0.shape[0]
+    counts = torch.zeros(w.n_layers, dtype=torch.int32, device="cuda")
+    idx_out = torch.zeros((w.n_layers, w.f), dtype=torch.int32, device="cuda")
+    xo, xl = ffn.decode_stack_layers(to_dev(x0), counts=counts, idx_out=idx_out)
+    torch.cuda.synchronize()
+    assert torch.equal(xo, xl[-1]), (tag, "last layer row differs from x_out")
+    xs = [x0.astype(np.float64)] + [xl[l].cpu().numpy().astype(np.float64) for l in range(w.n_layers)]
+    cg, ig = counts.cpu().numpy(), idx_out.cpu().numpy()
+    flips = 0
+    for l in range(w.n_layers):
+        Lo = layers[l][1]
+        u = oracle.rms_norm(xs[l])
+        pr = oracle.predict(u, Lo["p1_t"], Lo["p2_t"], Lo["b_pred"], w.pdtype, hot_prefix=hot_prefix)
+        gi = ig[l, : cg[l]]
+        assert np.all(np.diff(gi) > 0), (tag, l, "active list not ascending")
+        if hot_prefix:
+            H = min(hot_prefix, gi.size)
+            assert np.array_equal(gi[:H], np.arange(H)), (tag, l, "hot prefix missing")
+        diff = np.setxor1d(gi, pr["idx"])
+        assert np.all(band_mask(pr["z"])[diff]), (tag, l, f"{int((~band_mask(pr['z'])[diff]).sum())} out-of-band")
+        flips += int(diff.size > 0)
+        _, yo = oracle.sparse_ffn(u, Lo, gi, w.kind, w.wdtype)
+        err = rel_l2(xs[l + 1] - xs[l], yo)
+        assert err <= TOL[w.wdtype], (tag, l, err)
+    return xo.cpu().numpy(), flips

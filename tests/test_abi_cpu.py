@@ -85,3 +85,20 @@ def test_null_arguments(P):
     assert P._lib.pi_hot_first_order(None, 0, None, None) == 0          # empty order is a no-op
     assert P._lib.pi_permute_rows(None, None, None, -1, 16, None, None) == 1
     P._lib.pi_ffn_destroy(None)                                          # no-op
+
+
+def test_injected_descriptor_fault(P):
+    """PI_FAULT=badarg makes descriptor validation fail on the host: INVALID_ARG, no handle."""
+    desc = P.PiFfnDesc(512, 2048, 64, 1, 1, 0, 0, 0, 0.0)
+    os.environ["PI_FAULT"] = "badarg"
+    try:
+        rc, h = _create(P, desc, None)
+    finally:
+        del os.environ["PI_FAULT"]
+    assert rc == 1 and h is None
+    os.environ["PI_FAULT"] = "none-of-these"     # an unknown value injects nothing
+    try:
+        rc, h = _create(P, P.PiFfnDesc(500, 2048, 64, 1, 1, 0, 0, 0, 0.0), None)
+    finally:
+        del os.environ["PI_FAULT"]
+    assert rc == 1 and h is None                 # the real validation (d % 8) still runs
