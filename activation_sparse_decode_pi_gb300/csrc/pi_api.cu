@@ -179,14 +179,15 @@ struct pi_ffn {
     bool stack_ok = false;
     int n_hot = 0;                     // neurons [0, n_hot) expected to fire on most tokens
     int hot_prefix = 0;                // neurons [0, hot_prefix) computed on every token
-    int stack_p2 = 0;                  // owned P2 rows per CTA the persistent step stages in its ring
+    int stack_p2 = 0;                  // ring slots of the persistent step for 16-row tiles of owned P2 rows
     StackLayer *stack_layers = nullptr;
     uint32_t *stack_mask = nullptr;
     float *stack_sumsq = nullptr;
     int stack_slots = 0, stack_slot_bytes = 0;
     size_t stack_smem = 0;
     unsigned long long *phase_stamps = nullptr;   // pi_ffn_set_phase_trace (borrowed device buffer)
-    int off_ring = 0, off_flags = 0, off_mbar = 0, off_ua = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
+    int stack_pf = 0;                  // next-layer L2 prefetch of the persistent step (PI_FFN_STACK_PF)
+    int off_ring = 0, off_flags = 0, off_mbar = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
     // tensor-core path (batch >= tc_min_b)
     bool tc_ok = false;
     int tc_min_b = 16, tc_nbmax = 0, tc_rpad = 0, tc_fpad = 0;
@@ -618,14 +619,10 @@ void plan_stack(pi_ffn_t *h)
     const size_t sclb = D.wdtype == PI_INT4_G128 ? (size_t)(D.d / 128) * 2 : 0;
     const size_t slot = align_up(rows * (rowb + sclb) + 16, 128);
     const size_t own = (size_t)(D.f + P - 1) / P;
-    // u (phase A), hp (phase BC) and the reduction scratch (BC and D) are never live together
-    // with u: hp and the scratch share u's region when they fit in it.
-    const size_t off_ua = 0;
-    const size_t ua_end = align_up((size_t)D.d * 4, 128);
-    const bool share = align_up((size_t)D.r * 4, 128) + 8192 <= ua_end;
-    const size_t off_hp = share ? off_ua : ua_end;
-    const size_t off_scr = align_up(off_hp + (size_t)D.r * 4, 128);
-    const size_t off_flags = share ? ua_end : off_scr + 8192;
+    // hp (phase BC, also as its hi/lo halves), the reduction scratch (BC and D), the logit flags
+    const size_t off_hp = 0;
+    const size_t off_scr = align_up((size_t)D.r * 4, 128);
+    const size_t off_flags = off_scr + 8192;
     const size_t off_mbar = align_up(off_flags + own, 16);
     const size_t off_ring = align_up(off_mbar + 8 * STACK_MAX_SLOTS, 128);
     int optin = 0;
@@ -639,20 +636,28 @@ void plan_stack(pi_ffn_t *h)
     h->stack_slots = (int)std::min((size_t)STACK_MAX_SLOTS, ring / slot);
     h->stack_slot_bytes = (int)slot;
     h->stack_ring = (int)((size_t)h->stack_slots * slot);
-    h->off_ua = (int)off_ua;
     h->off_hp = (int)off_hp;
     h->off_scr = (int)off_scr;
     h->off_ring = (int)off_ring;
     h->off_flags = (int)off_flags;
     h->off_mbar = (int)off_mbar;
-    // The ring is idle from the end of one layer's FFN to the next layer's logits: the next
-    // layer's owned P2 rows are copied into it then, as many as fit (PI_FFN_STACK_P2=0: none).
-    // Between layers they may also take the rest of the shared memory past the last slot.
+    // The owned P2 rows pass through the ring in 16-row tiles: the first ones are copied in while
+    // the ring is idle between one layer's FFN and the next layer's logits, and the logits stream
+    // the rest through the same slots. A tile slot may reach past the last FFN slot, into the rest
+    // of the shared memory (PI_FFN_STACK_P2=0: no tiles, the logits read P2 from memory).
     const char *p2env = std::getenv("PI_FFN_STACK_P2");
     const size_t p2row = elt_row_bytes(D.pdtype, D.r), p2st = (size_t)stack_p2_stride((int)p2row);
     h->stack_p2 = 0;
-    if (!(p2env && p2env[0] == '0') && p2row % 16 == 0) h->stack_p2 = (int)std::min(own, ring / p2st);
-    h->stack_smem = off_ring + std::max((size_t)h->stack_ring, (size_t)h->stack_p2 * p2st);
+    if (!(p2env && p2env[0] == '0') && p2row % 16 == 0)
+        h->stack_p2 = (int)std::min({(size_t)STACK_P2_TILES, ring / (16 * p2st), (own + 15) / 16});
+    h->stack_smem = off_ring + std::max((size_t)h->stack_ring, (size_t)h->stack_p2 * 16 * p2st);
+    // The next layer's predictor rows are prefetched into L2 a layer ahead only while one layer's
+    // predictor is small next to L2 (129 MB): a larger one is evicted by the layer's own traffic
+    // before it is read, and the prefetch then costs its bytes twice (measured on the OPT-175B
+    // shape: 1.31x the algorithmic DRAM bytes, 13% slower).
+    const size_t pred_bytes = elt_row_bytes(D.pdtype, D.d) * D.r + p2row * D.f;
+    h->stack_pf = pred_bytes <= (40u << 20) ? 2 : 0;
+    if (const char *pf = std::getenv("PI_FFN_STACK_PF")) h->stack_pf = std::max(0, std::min(2, std::atoi(pf)));
     h->stack_ok = true;
 }
 
@@ -685,7 +690,6 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.nblocks = (unsigned)h->nsm;
     const long long pbytes = (D.pdtype == PI_F32 ? 4LL : 2LL) * ((long long)D.r * D.d + (long long)D.f * D.r);
     a.pf_bytes = std::min(pbytes, 48LL << 20);
-    a.off_ua = h->off_ua;
     a.off_hp = h->off_hp;
     a.off_scr = h->off_scr;
     a.off_ring = h->off_ring;
@@ -695,7 +699,8 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.hot_prefix = h->hot_prefix;
     a.hot_k = h->n_hot > 0 ? std::min((h->n_hot + h->nsm - 1) / h->nsm, h->stack_slots - 2) : 0;
     if (a.hot_k < 0) a.hot_k = 0;
-    a.p2_stage = a.hot_k > 0 ? 0 : h->stack_p2;   // the hot slots hold the ring between layers
+    a.p2_tiles = a.hot_k > 0 ? 0 : h->stack_p2;   // the hot slots hold the ring between layers
+    a.pf = h->stack_pf;
     a.x_layers = x_layers;
     a.stamps = h->phase_stamps;
     a.bias_bulk = D.f % 4 == 0 ? 1 : 0;

@@ -138,13 +138,16 @@ __device__ __forceinline__ unsigned long long barrier_base(const unsigned long l
     return c - c % per_launch;
 }
 
-// Bulk copies a CTA may have in flight at a grid barrier: phase par[0] of *one (if >= 0) and
-// phase par[1] of each of many[0..nmany) (if >= 0). par lives in shared memory.
+// Bulk copies a CTA may have in flight at a grid barrier: phase tile_par[k] of tiles[k] for
+// k < ntiles (where >= 0), and phase *many_par of each of many[0..nmany) (if >= 0). The
+// parities live in shared memory.
 struct PendingCopies {
-    uint64_t *one;
+    uint64_t *tiles;
+    const int *tile_par;
+    int ntiles;
     uint64_t *many;
     int nmany;
-    const int *par;
+    const int *many_par;
 };
 
 struct NoWork {
@@ -170,9 +173,12 @@ __device__ __forceinline__ bool grid_sync_to(unsigned long long *cnt, unsigned l
                 if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
                     set_status(status, ST_TIMEOUT);
                     ok = 0;
-                    if (pc && pc->par[0] >= 0) mbar_wait(pc->one, (uint32_t)pc->par[0]);
-                    if (pc && pc->par[1] >= 0)
-                        for (int k = 0; k < pc->nmany; ++k) mbar_wait(&pc->many[k], (uint32_t)pc->par[1]);
+                    if (pc) {
+                        for (int k = 0; k < pc->ntiles; ++k)
+                            if (pc->tile_par[k] >= 0) mbar_wait(&pc->tiles[k], (uint32_t)pc->tile_par[k]);
+                        if (*pc->many_par >= 0)
+                            for (int k = 0; k < pc->nmany; ++k) mbar_wait(&pc->many[k], (uint32_t)*pc->many_par);
+                    }
                     break;
                 }
                 __nanosleep(64);   // fewer polls on the counter's line while the arrivals land

@@ -46,6 +46,7 @@ constexpr int STACK_SLICE = 32;           // output columns per reduction slice
 constexpr int STACK_MAX_CHUNK = 512;      // neurons one CTA may own (f <= 512 * grid)
 constexpr int STACK_MAX_SLOTS = 16;       // shared-memory ring slots (one neuron's rows each)
 constexpr int STACK_MAX_P1_ROWS = 8;      // predictor hidden units one CTA owns (r <= 8 * SMs)
+constexpr int STACK_P2_TILES = 16;        // ring slots for 16-row tiles of owned P2 rows, at most
 
 struct StackLayer {
     const void *wg, *wu, *wd;     // [f x d] gate (W1), up (NULL if non-gated), W_down transposed
@@ -79,12 +80,13 @@ struct StackArgs {
     int slots, slot_bytes;
     unsigned nblocks;             // CTAs expected at every grid barrier
     long long pf_bytes;           // next-layer predictor bytes to prefetch into L2
-    int off_ua, off_hp, off_scr, off_flags, off_mbar, off_ring;   // dynamic shared-memory layout
+    int off_hp, off_scr, off_flags, off_mbar, off_ring;   // dynamic shared-memory layout
     int ring_bytes;               // ring region: the neuron slots
     int bias_bulk;                // gate biases ride in the row copies (every layer has one and f % 4 == 0)
     int hot_k;                    // ring slots per CTA held by hot owned neurons (loaded a layer ahead), <= slots - 2
     int hot_prefix;               // neurons below this are active without a logit
-    int p2_stage;                 // owned P2 rows per CTA copied into the ring ahead of their layer (0: none)
+    int p2_tiles;                 // ring slots for 16-row tiles of owned P2 rows (0: none)
+    int pf;                       // next-layer L2 prefetch: 0 none, 1 P1 rows, 2 P1 and the unstaged P2 rows
     float *x_layers;              // optional [L x d]: row l = x_{l+1} (every layer's output), or NULL
     unsigned long long *stamps;   // optional [L x STACK_PHASES x grid] %globaltimer stamps, or NULL
 };

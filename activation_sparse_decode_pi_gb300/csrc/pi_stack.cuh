@@ -6,8 +6,9 @@
 // 512 threads that walks all layers. A layer is three phases separated by bounded
 // grid barriers:
 //
-//   A   hp[k] = ReLU(inv * P1T[k] . x)      CTA c: hidden units [c*r/P, (c+1)*r/P); x is
-//       staged unscaled while the RMS scale inv is summed from the slices' sums of squares
+//   A   hp[k] = ReLU(inv * P1T[k] . x)      CTA c: hidden units [c*r/P, (c+1)*r/P); each lane
+//       reads the x chunks of the P1 chunks it multiplies (from L2) while the RMS scale inv is
+//       summed from the slices' sums of squares
 //   -- barrier
 //   BC  CTA c owns the neurons i = c, c+P, c+2P, ... (hot-first order spreads the hot
 //       neurons evenly). It computes their logits z[i] = hp . P2T[i] + b_p[i], keeps the
@@ -26,10 +27,11 @@
 // counts (and, on request, the ascending active lists) are produced alongside.
 // The predictor weights do not depend on the input. The ring is idle between one layer's
 // FFN and the next layer's logits, so the next layer's owned P2 rows are copied into it
-// then (as many as fit); the logits of a CTA whose rows all fit run as 16-row tiles on the
-// tensor cores (mma.sync, hp split into hi and lo halves of the predictor's type), the
-// others as CUDA-core row dot products. P1 and the P2 rows that do not fit are prefetched
-// into L2 a layer ahead.
+// then (as many as fit); with a 16-bit predictor (r % 32 == 0) the logits run as 16-row tiles
+// on the tensor cores (mma.sync, hp split into hi and lo halves of the predictor's type),
+// staged rows read from shared memory and the others streamed from memory; otherwise as
+// CUDA-core row dot products. While one layer's predictor is small next to L2, P1 and the P2
+// rows that do not fit are prefetched into L2 a layer ahead.
 // Hot neurons (the first hot_k owned ones in hot-first order, typically active on most
 // tokens) can have ring slots of their own: their rows are requested one layer ahead, during
 // the previous layer's barrier wait, before the predictor has said whether they fire. A hot
@@ -207,7 +209,6 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *ring = smem + a.off_ring;                 // neuron slots
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + a.off_mbar);
-    float4 *ua4 = reinterpret_cast<float4 *>(smem + a.off_ua);         // phase A: u (planar, predictor type)
     float4 *hp4 = reinterpret_cast<float4 *>(smem + a.off_hp);         // phase BC: hp (planar)
     float4 *scr4 = reinterpret_cast<float4 *>(smem + a.off_scr);       // phase D: partial sums
     unsigned char *sflag = smem + a.off_flags;                          // phase BC: logit > tau per owned row
@@ -219,11 +220,12 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     __shared__ float sbias[STACK_MAX_CHUNK];
     __shared__ float s_inv;
     __shared__ int s_flag;
-    __shared__ uint64_t s_p2bar;   // the staged P2 rows of the next layer have landed
+    __shared__ uint64_t s_p2bar[STACK_P2_TILES];   // P2 tile slot j: its rows have landed
+    __shared__ int s_p2use[STACK_P2_TILES];        // tiles slot j holds per layer
+    __shared__ int s_p2par[STACK_P2_TILES];        // parity of slot j's copies in flight across a grid barrier (-1: none)
     __shared__ float spb[STACK_MAX_CHUNK];   // predictor bias of the owned rows, copied during phase A
     __shared__ const void *s_p2next;          // P2 of the next layer (read during phase A)
-    __shared__ int s_pend[2];      // thread 0: parity of staged P2 copies not yet waited for, of the
-                                   // last hot-slot copies issued (-1: none)
+    __shared__ int s_pend;         // parity of the last hot-slot copies issued (-1: none)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x, c = blockIdx.x;
@@ -237,12 +239,39 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     const int K = c < f ? (f - 1 - c) / P + 1 : 0;          // owned neurons: i = c + P * k, k < K
     const int bias_off = ROWS * (rowb + sclb);               // 16-byte chunk holding the gate bias
     const bool bias_bulk = a.bias_bulk != 0;                 // the chunk stays inside b_gate only if f % 4 == 0
-    // Owned P2 rows k < KS of the next layer are copied into the ring once this layer's FFN is
-    // done with it (row k at ring + k * p2st); they land during the reduction and predictor
-    // phases, so the logits read them from shared memory. Rows below the hot prefix need none.
+    // The owned P2 rows pass through the ring in tiles of 16 rows: tile t (owned rows
+    // [16t, 16t + 16)) in slot t % RT at ring + (t % RT) * 16 * p2st, completing on mbarrier
+    // s_p2bar[t % RT]. The ring is idle from the end of one layer's FFN to the next layer's
+    // logits, so the first NI = min(MT, RT) tiles of the next layer are copied into it then (they
+    // land during the reduction and predictor phases). With the tensor-core logits and more tiles
+    // than slots, the logits stream the rest: each slot is refilled with the tile RT further on
+    // as soon as its tile has been multiplied. Rows below the hot prefix need no copy.
     const int p2b = r * pb, p2st = stack_p2_stride(p2b);
-    const int KS = min(K, a.p2_stage);
-    const int ks0 = a.hot_prefix > c ? min(KS, (a.hot_prefix - c + P - 1) / P) : 0;
+    const int MT = (K + 15) >> 4, RT = a.p2_tiles;
+    bool TCL = false;   // logits on the tensor cores
+    if constexpr (PT == DT_BF16 || PT == DT_F16) TCL = K > 0 && (r & 15) == 0 && (MT <= RT || RT >= 2);
+    const int NI = min(MT, RT);
+    const int MTS = TCL ? MT : NI;                           // tiles through the ring per layer
+    const int KS = min(K, NI * 16);                          // rows staged between layers
+    const int ks0 = a.hot_prefix > c ? min(K, (a.hot_prefix - c + P - 1) / P) : 0;
+    // bytes of tile t's rows that are copied (past K and below the hot prefix: none)
+    auto tile_bytes = [&](int t) -> uint32_t {
+        const int lo = max(16 * t, ks0), hi = min(16 * t + 16, K);
+        return hi > lo ? (uint32_t)((hi - lo) * p2b) : 0u;
+    };
+    // parity of the phase of slot t % RT that holds tile t of layer l
+    auto tile_par = [&](int l, int t) -> uint32_t {
+        const int j = t % RT;
+        return (uint32_t)(l * s_p2use[j] + t / RT) & 1u;
+    };
+    // copy rows [lo, hi) of tile t (owned rows) into its slot; the ring there is free
+    auto copy_tile_rows = [&](const void *p2, int t, int j, int lo, int hi) {
+        for (int k = max(lo, ks0); k < hi && k < K; ++k) {
+            fence_proxy_async_smem();
+            bulk_g2s(ring + (size_t)(j * 16 + (k - 16 * t)) * p2st,
+                     (const char *)p2 + (size_t)(c + (size_t)P * k) * p2b, (uint32_t)p2b, &s_p2bar[j]);
+        }
+    };
     // Ring slots [0, HK) hold this CTA's hot owned neurons k < HK (loaded every layer before its
     // predictor runs: the copy for layer l is the slot's l-th, parity l & 1). Slots [HK, S) take
     // the other active neurons in list order: the cold neuron staged n-th in this launch goes to
@@ -255,22 +284,27 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     };
     auto sync_grid = [&](auto work) -> bool {
         ++kb;
-        const PendingCopies pc{&s_p2bar, mbar, min(a.hot_k, K), s_pend};
+        const PendingCopies pc{s_p2bar, s_p2par, NI, mbar, min(a.hot_k, K), &s_pend};
         return grid_sync_to(a.bar, s_base + (unsigned long long)kb * a.nblocks, a.status, &s_flag, &pc, work);
     };
     const NoWork no_work;
-    auto expect_p2 = [&]() {
-        if (tid == 0) mbar_arrive_expect_tx(&s_p2bar, (uint32_t)((KS - ks0) * p2b));
+    // the first NI tiles of layer l are about to be staged: their byte counts, and their parities
+    // for a drain after a timed-out grid barrier
+    auto expect_p2 = [&](int l) {
+        if (tid < NI) {
+            mbar_arrive_expect_tx(&s_p2bar[tid], tile_bytes(tid));
+            s_p2par[tid] = (int)tile_par(l, tid);
+        }
     };
     // one copy per thread, row k = 16 * lane + warp (a warp's copies are issued one after another,
     // so every warp takes a few); the ring is free and expect_p2 ran
     auto stage_p2 = [&](const void *p2) {
         const int k = lane * SNW + warp;
-        if (k >= ks0 && k < KS) {
-            fence_proxy_async_smem();
-            bulk_g2s(ring + (size_t)k * p2st, (const char *)p2 + (size_t)(c + (size_t)P * k) * p2b, (uint32_t)p2b,
-                     &s_p2bar);
-        }
+        if (k < KS) copy_tile_rows(p2, k >> 4, k >> 4, k, k + 1);   // tile k / 16 < NI sits in slot k / 16
+    };
+    // after a timeout: wait (bounded) for the copies of tiles [t0, t1) of layer l
+    auto drain_tiles = [&](int l, int t0, int t1) {
+        for (int t = t0; t < t1 && t < MTS; ++t) mbar_wait(&s_p2bar[t % RT], tile_par(l, t));
     };
 
     // this CTA's P1 rows, one chunk per lane and row at a time
@@ -280,8 +314,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     // the rest of this CTA's predictor slice, into L2
     // (one prefetch per thread: thread k in [KS, K) takes owned P2 row k, the last thread the P1 rows)
     auto prefetch_predictor = [&](const StackLayer &L) {
-        if (tid >= KS && tid < K) prefetch_l2((const char *)L.p2 + (size_t)(c + (size_t)P * tid) * r * pb, r * pb);
-        if (tid == STACK_NT - 1) prefetch_l2_range((const char *)L.p1 + (size_t)k0 * d * pb, (size_t)(k1 - k0) * d * pb);
+        if (a.pf >= 2 && tid >= KS && tid < K)
+            prefetch_l2((const char *)L.p2 + (size_t)(c + (size_t)P * tid) * r * pb, r * pb);
+        if (a.pf >= 1 && tid == STACK_NT - 1)
+            prefetch_l2_range((const char *)L.p1 + (size_t)k0 * d * pb, (size_t)(k1 - k0) * d * pb);
     };
 
     // the hot owned neurons of layer Lw into their slots, one issuing thread per neuron; the
@@ -302,13 +338,17 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     // ---------------------------------------------------------------- phase 0
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&mbar[s], 1);
-        mbar_init(&s_p2bar, 1);
+        for (int j = 0; j < RT && j < STACK_P2_TILES; ++j) mbar_init(&s_p2bar[j], 1);
         fence_mbar_init();
-        s_pend[0] = KS > 0 ? 0 : -1;
-        s_pend[1] = a.hot_k > 0 ? 0 : -1;
+        s_pend = a.hot_k > 0 ? 0 : -1;
         s_base = barrier_base(a.bar, (unsigned long long)(3 * a.L) * a.nblocks);
     }
-    if (KS > 0) expect_p2();
+    if (tid < STACK_P2_TILES) {
+        s_p2use[tid] = tid < min(MTS, RT) ? (MTS - tid + RT - 1) / RT : 0;
+        s_p2par[tid] = -1;
+    }
+    __syncthreads();   // the barriers are initialised and s_p2use is set
+    expect_p2(0);
     prefetch_predictor(a.layers[0]);
     __syncthreads();
     issue_hot(a.layers[0], -1);
@@ -343,40 +383,34 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 
         // ------------------------------------------------------------ A: predictor hidden layer
         {
-            // The first chunks of this CTA's P1 rows (prefetched into L2 a layer ago) are requested
-            // first. x_l is staged unscaled while warp 0 adds up the slices' sums of squares, both
-            // reads in flight together; the scale is applied to the dot products (hp = ReLU(inv * P1 x)).
+            // The first chunks of this CTA's P1 rows (prefetched into L2 a layer ago where that pays)
+            // are requested with the matching chunks of x_l (read from L2, unscaled), while warp 0
+            // adds up the slices' sums of squares; the RMS scale is applied to the dot products
+            // (hp = ReLU(inv * P1 x)). x is not staged in shared memory: each lane reads the x chunk
+            // of the P1 chunk it multiplies, which the 8 rows share.
             constexpr int QP = VP / 4;
-            constexpr int XQ = CPT * VW / 4;   // float4 of x per thread: d <= CPT * STACK_NT * VW
-            float4 xv[XQ];
+            float4 xq[QP];
+            auto load_x = [&](int ci) {
 #pragma unroll
-            for (int q = 0; q < XQ; ++q) {
-                const int t = tid + q * STACK_NT;
-                xv[q] = t < d / 4 ? __ldcg(reinterpret_cast<const float4 *>(xl) + t) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+                for (int q = 0; q < QP; ++q)
+                    xq[q] = ci < pa_ce ? __ldcg(reinterpret_cast<const float4 *>(xl + (size_t)ci * VP) + q)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            };
+            load_p1_chunk<PT>(pa, Lw.p1, k0, k1, nchp, pa_cb + lane, pa_ce);
+            load_x(pa_cb + lane);
             const int nsl = (d + STACK_SLICE - 1) / STACK_SLICE;
             float ssq = 0.f;
             if (l > 0 && warp == 0)
                 for (int s = lane; s < nsl; s += 32) ssq += __ldcg(a.sumsq + s);
-            load_p1_chunk<PT>(pa, Lw.p1, k0, k1, nchp, pa_cb + lane, pa_ce);   // after x: its reads come back first
             if (tid < K) {   // the logits' biases, waited for before this phase's grid barrier
                 if (Lw.bp) cp_async4(&spb[tid], Lw.bp + c + P * tid);
                 else spb[tid] = 0.f;
             }
             if (tid == STACK_NT - 1 && l + 1 < a.L) s_p2next = a.layers[l + 1].p2;
-#pragma unroll
-            for (int q = 0; q < XQ; ++q) {
-                const int t = tid + q * STACK_NT;
-                if (t >= d / 4) break;
-                const int ci = t / QP, qq = t - ci * QP;
-                ua4[qq * nchp + ci] = xv[q];
-            }
             if (l > 0 && warp == 0) {
                 ssq = warp_sum(ssq);
                 if (lane == 0) s_inv = 1.0f / sqrtf(ssq / (float)d + a.eps);
             }
-            __syncthreads();
-            inv = s_inv;
             if (l + 1 < a.L) prefetch_predictor(a.layers[l + 1]);
             const uint4 *row[8];
             const __half *srow[8];
@@ -388,11 +422,35 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             float acc[8][1];
 #pragma unroll
             for (int k = 0; k < 8; ++k) acc[k][0] = 0.f;
-            rows_consume<PT, 8, 1, 1>(pa, pa_cb + lane, pa_ce, ua4, d, acc);
+            // acc[k] += P1 row k0 + k, chunk ci . x chunk ci (the loaded ones)
+            auto consume = [&](int ci) {
+                if (ci >= pa_ce) return;
+                float xe[VP];
+#pragma unroll
+                for (int q = 0; q < QP; ++q) {
+                    xe[4 * q + 0] = xq[q].x;
+                    xe[4 * q + 1] = xq[q].y;
+                    xe[4 * q + 2] = xq[q].z;
+                    xe[4 * q + 3] = xq[q].w;
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    float wf[VP];
+                    unpack<PT>(pa.w[k][0], wf);
+                    float v = acc[k][0];
+#pragma unroll
+                    for (int e = 0; e < VP; ++e) v = fmaf(wf[e], xe[e], v);
+                    acc[k][0] = v;
+                }
+            };
+            consume(pa_cb + lane);
             for (int cc = pa_cb + lane + 32; cc < pa_ce; cc += 32) {
                 rows_issue(pa, row, srow, cc, pa_ce);
-                rows_consume<PT, 8, 1, 1>(pa, cc, pa_ce, ua4, d, acc);
+                load_x(cc);
+                consume(cc);
             }
+            __syncthreads();   // s_inv
+            inv = s_inv;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const float v = warp_sum(acc[k][0]);
@@ -443,26 +501,24 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 const int t = tid + u * STACK_NT;
                 hv[u] = t < r4 ? __ldcg(reinterpret_cast<const float4 *>(a.hp) + t) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            const bool p2ok = KS == 0 || mbar_wait(&s_p2bar, (uint32_t)l & 1u);
-            // joint decision: every thread saw the staged rows land, or the CTA leaves
-            auto staged_ok = [&]() -> bool {
-                if (__syncthreads_and(p2ok)) {
-                    if (tid == 0) s_pend[0] = -1;
-                    return true;
-                }
+            // the staged tiles [0, nt) have landed (every thread waits); false after a timeout, when
+            // the CTA leaves once its copies in flight have landed
+            auto wait_staged = [&](int nt) -> bool {
+                bool ok = true;
+                for (int j = 0; j < nt; ++j) ok = mbar_wait(&s_p2bar[j], tile_par(l, j)) && ok;
+                if (__syncthreads_and(ok)) return true;
                 if (tid == 0) {
                     set_status(a.status, ST_TIMEOUT);
-                    mbar_wait(&s_p2bar, (uint32_t)l & 1u);
+                    drain_tiles(l, 0, nt);
                 }
                 return false;
             };
-            // Every owned row staged and 16-bit: the logits are one small contraction on the tensor
-            // cores, [16-row tile of P2 rows] x [hp_hi hp_lo 0 ... 0] per mma.sync, hp entering as
-            // hi + lo halves in the predictor's type (so ~16 bits of it, with fp32 accumulation).
-            bool tcl = false;
-            if constexpr (PT == DT_BF16 || PT == DT_F16) tcl = KS == K && K > 0 && (r & 15) == 0;
+            // 16-bit predictor, r % 16 == 0: the logits are small contractions on the tensor cores,
+            // [16-row tile of P2 rows] x [hp_hi hp_lo 0 ... 0] per mma.sync, hp entering as hi + lo
+            // halves in the predictor's type (so ~16 bits of it, with fp32 accumulation), A read
+            // from the ring with ldmatrix (the odd row stride keeps it conflict-free).
             bool act = false;   // owned neuron k = tid fires
-            if (tcl) {
+            if (TCL) {
                 uint32_t *bfr = reinterpret_cast<uint32_t *>(hp4);   // B fragments [r/16][8 lanes][2]
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
@@ -480,19 +536,13 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                         bfr[(s16 * 8 + ln + 4) * 2 + reg] = (uint32_t)l0 | ((uint32_t)l1 << 16);
                     }
                 }
-                if (!staged_ok()) return;
-                // units (tile t, k part g): G warps share a tile when there are fewer tiles than warps
                 float *zp = reinterpret_cast<float *>(scr4);
-                const int MT = (K + 15) >> 4, NKS = r >> 4;
-                const int G = MT >= SNW ? 1 : SNW / MT;
-                for (int u = warp; u < MT * G; u += SNW) {
-                    const int t = u / G, g = u - t * G;
-                    const int s0 = g * NKS / G, s1 = (g + 1) * NKS / G;
-                    const int rw = min(t * 16 + (lane & 15), K - 1);   // rows past K repeat row K - 1
-                    const uint32_t ab = smem_u32(ring) + (uint32_t)(rw * p2st) + (uint32_t)(lane >> 4) * 16u;
-                    // two accumulators (even and odd k steps), so consecutive products do not wait
-                    // on each other
-                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                const int NKS = r >> 4;
+                // the products of k16 steps [s0, s1) of the 16 rows of the tile in slot j (rows past
+                // K repeat row K - 1) into two accumulators (even and odd steps)
+                auto tile_mma = [&](int t, int j, int s0, int s1, float (&acc)[2][4]) {
+                    const int rw = min(t * 16 + (lane & 15), K - 1) - t * 16;
+                    const uint32_t ab = smem_u32(ring) + (uint32_t)((j * 16 + rw) * p2st) + (uint32_t)(lane >> 4) * 16u;
                     for (int s16 = s0; s16 < s1; s16 += 2) {
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
@@ -504,19 +554,75 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                             mma_16816<PT>(acc[e], af, bf.x, bf.y);
                         }
                     }
-                    if ((lane & 3) == 0) {   // columns 0 (hi part) and 1 (lo part) of rows lane/4, lane/4 + 8
-                        zp[u * 16 + (lane >> 2)] = (acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1]);
-                        zp[u * 16 + (lane >> 2) + 8] = (acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3]);
+                };
+                if (MT <= RT) {
+                    // every tile was staged between layers: one pass, units (tile t, k part g), G warps
+                    // sharing a tile when there are fewer tiles than warps
+                    if (!wait_staged(MT)) return;
+                    const int G = MT >= SNW ? 1 : SNW / MT;
+                    for (int u = warp; u < MT * G; u += SNW) {
+                        const int t = u / G, g = u - t * G;
+                        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                        tile_mma(t, t, g * NKS / G, (g + 1) * NKS / G, acc);
+                        if ((lane & 3) == 0) {   // columns 0 (hi part) and 1 (lo part) of rows lane/4, lane/4 + 8
+                            zp[u * 16 + (lane >> 2)] = (acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1]);
+                            zp[u * 16 + (lane >> 2) + 8] = (acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3]);
+                        }
+                    }
+                    __syncthreads();
+                    if (tid < K) {
+                        const int t = tid >> 4;
+                        float z = 0.f;
+                        for (int g = 0; g < G; ++g) z += zp[(t * G + g) * 16 + (tid & 15)];   // fixed order
+                        z += spb[tid];
+                        act = c + P * tid < a.hot_prefix || z > a.tau;
+                    }
+                } else {
+                    // more tiles than slots: tile by tile, every warp taking a 1/16 share of its k
+                    // steps; the slot is refilled with the tile RT further on once the tile's products
+                    // are done, so up to RT - 1 tiles of copies stay in flight
+                    float *zt = sbias;   // the tiles' logits (sbias is written only after the list)
+                    const int s0 = warp * NKS / SNW, s1 = (warp + 1) * NKS / SNW;
+                    int j = 0, wrap = 0;   // slot of tile t, and t / RT
+                    for (int t = 0; t < MT; ++t) {
+                        const bool ok = mbar_wait(&s_p2bar[j], (uint32_t)(l * s_p2use[j] + wrap) & 1u);
+                        if (!__syncthreads_and(ok)) {
+                            if (tid == 0) {
+                                set_status(a.status, ST_TIMEOUT);
+                                drain_tiles(l, t, t + RT);
+                            }
+                            return;
+                        }
+                        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                        tile_mma(t, j, s0, s1, acc);
+                        float *zb = zp + (t & 1) * (SNW * 16);   // double-buffered partials
+                        if ((lane & 3) == 0) {
+                            zb[warp * 16 + (lane >> 2)] = (acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1]);
+                            zb[warp * 16 + (lane >> 2) + 8] = (acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3]);
+                        }
+                        __syncthreads();   // the slot's rows are read and the partials written
+                        if (tid < 16) {
+                            float z = 0.f;
+                            for (int w = 0; w < SNW; ++w) z += zb[w * 16 + tid];   // fixed order
+                            zt[t * 16 + tid] = z;
+                        }
+                        const int tn = t + RT;
+                        if (tn < MT) {   // refill: one thread registers the bytes, 16 threads copy a row each
+                            if (tid == 32) mbar_arrive_expect_tx(&s_p2bar[j], tile_bytes(tn));
+                            if (tid >= 64 && tid < 80) copy_tile_rows(Lw.p2, tn, j, tn * 16 + tid - 64, tn * 16 + tid - 63);
+                        }
+                        if (++j == RT) {
+                            j = 0;
+                            ++wrap;
+                        }
+                    }
+                    __syncthreads();
+                    if (tid < K) {
+                        const float z = zt[tid] + spb[tid];
+                        act = c + P * tid < a.hot_prefix || z > a.tau;
                     }
                 }
-                __syncthreads();
-                if (tid < K) {
-                    const int t = tid >> 4;
-                    float z = 0.f;
-                    for (int g = 0; g < G; ++g) z += zp[(t * G + g) * 16 + (tid & 15)];   // fixed order
-                    z += spb[tid];
-                    act = c + P * tid < a.hot_prefix || z > a.tau;
-                }
+                if (tid < NI) s_p2par[tid] = -1;   // every staged copy has been waited for
             } else {
                 rows_at(warp);
                 issue_rows(lane);                                    // before hp is staged
@@ -526,7 +632,8 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     const int t = tid + u * STACK_NT;
                     if (t < r4) hp4[(t % QH) * nchr + t / QH] = hv[u];   // planar layout of the row dot products
                 }
-                if (!staged_ok()) return;
+                if (!wait_staged(NI)) return;
+                if (tid < NI) s_p2par[tid] = -1;
                 for (int kbase = warp; kbase < K; kbase += SNW * 5) {
                     if (kbase != warp) {
                         rows_at(kbase);
@@ -775,11 +882,8 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
         // rows (a whole layer before their predictor runs) or its staged P2 rows are requested
         // while this CTA waits for the others.
         if (l + 1 < a.L) {
-            if (KS > 0) expect_p2();
-            if (tid == 0) {
-                if (a.hot_k > 0) s_pend[1] = (l + 1) & 1;
-                if (KS > 0) s_pend[0] = (l + 1) & 1;
-            }
+            expect_p2(l + 1);
+            if (tid == 0 && a.hot_k > 0) s_pend = (l + 1) & 1;
         }
         if (!sync_grid([&] {
                 if (l + 1 < a.L && a.hot_k > 0) issue_hot(a.layers[l + 1], l);
@@ -790,38 +894,58 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 
         // ------------------------------------------------------------ D: fixed-order reduction + residual
         {
+            // Up to four of this CTA's slices at a time, every partial load of them in flight together.
+            // Thread (g, c4) adds partials g, g + 64, ... of float4 column c4; the 64 groups are then
+            // added in a fixed tree (4 per warp by shuffles, 16 warps through shared memory).
             const int nsl = (d + STACK_SLICE - 1) / STACK_SLICE;
             const int c4 = tid & 7, g = tid >> 3;   // 8 float4 per slice, 64 groups of partials
-            for (int s = c; s < nsl; s += P) {
-                const int col = s * STACK_SLICE + c4 * 4;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (col < d) {
+            float4 *red4 = scr4;                   // [16 warps][4 slices][8 columns]
+            for (int s0 = c; s0 < nsl; s0 += 4 * P) {
+                float4 acc[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int col = (s0 + j * P) * STACK_SLICE + c4 * 4;
+                    if (s0 + j * P < nsl && col < d) {
 #pragma unroll 3
-                    for (int q = g; q < P; q += STACK_NT / 8) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part + (size_t)q * d + col));
-                        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+                        for (int q = g; q < P; q += STACK_NT / 8) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part + (size_t)q * d + col));
+                            acc[j].x += v.x; acc[j].y += v.y; acc[j].z += v.z; acc[j].w += v.w;
+                        }
                     }
                 }
-                scr4[g * 8 + c4] = acc;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {   // lanes l, l ^ 8, l ^ 16, l ^ 24: the warp's 4 groups
+#pragma unroll
+                    for (int o = 8; o <= 16; o <<= 1) {
+                        acc[j].x += __shfl_xor_sync(0xffffffffu, acc[j].x, o);
+                        acc[j].y += __shfl_xor_sync(0xffffffffu, acc[j].y, o);
+                        acc[j].z += __shfl_xor_sync(0xffffffffu, acc[j].z, o);
+                        acc[j].w += __shfl_xor_sync(0xffffffffu, acc[j].w, o);
+                    }
+                    if (lane < 8) red4[(warp * 4 + j) * 8 + lane] = acc[j];
+                }
                 __syncthreads();
-                if (tid < 8) {
+                if (tid < 32) {   // slice j = tid / 8, column c4
+                    const int j = tid >> 3, s = s0 + j * P;
+                    const int col = s * STACK_SLICE + c4 * 4;
                     float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int gg = 0; gg < STACK_NT / 8; ++gg) {   // fixed order
-                        const float4 v = scr4[gg * 8 + tid];
+                    for (int w = 0; w < SNW; ++w) {   // fixed order
+                        const float4 v = red4[(w * 4 + j) * 8 + c4];
                         y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
                     }
                     float ss = 0.f;
-                    if (col < d) {
+                    if (s < nsl && col < d) {
                         const float4 xv = __ldcg(reinterpret_cast<const float4 *>(xl + col));
                         y.x += xv.x; y.y += xv.y; y.z += xv.z; y.w += xv.w;
                         *reinterpret_cast<float4 *>(xn + col) = y;
                         if (a.x_layers) *reinterpret_cast<float4 *>(a.x_layers + (size_t)l * d + col) = y;
                         ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
                     }
-                    ss += __shfl_xor_sync(0xffu, ss, 1);
-                    ss += __shfl_xor_sync(0xffu, ss, 2);
-                    ss += __shfl_xor_sync(0xffu, ss, 4);
-                    if (tid == 0) a.sumsq[s] = ss;
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+                    if (c4 == 0 && s < nsl) a.sumsq[s] = ss;
                 }
                 __syncthreads();
             }

@@ -140,6 +140,14 @@ __device__ __forceinline__ void named_sync(int id, int n)
 template <int WT>
 __device__ __forceinline__ void split16(float x, uint16_t &hi, uint16_t &lo);
 
+// fp32 operands never take the 16-bit tensor-core paths; this only completes the set
+template <>
+__device__ __forceinline__ void split16<DT_F32>(float, uint16_t &hi, uint16_t &lo)
+{
+    hi = 0;
+    lo = 0;
+}
+
 template <>
 __device__ __forceinline__ void split16<DT_BF16>(float x, uint16_t &hi, uint16_t &lo)
 {

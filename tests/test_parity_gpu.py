@@ -276,10 +276,9 @@ def _handle(P, w, layers, stack_kernel: bool):
             os.environ["PI_FFN_STACK_KERNEL"] = old
 
 
-# r % 16 == 0 with 16-bit predictor weights: a CTA whose owned P2 rows are all staged in
-# shared memory computes its logits on the tensor cores (mma.sync); r = 136 keeps them on
-# the CUDA cores
-STACK_SHAPE_TC = dict(d=2048, f=3001, r=144)
+# r % 32 == 0 with 16-bit predictor weights: the logits run on the tensor cores (mma.sync,
+# staged rows from shared memory, the rest from memory); r = 136 keeps them on the CUDA cores
+STACK_SHAPE_TC = dict(d=2048, f=3001, r=160)
 # d * 4 bytes >= r * 4 + 8 KB: hp and the reduction scratch share u's shared-memory region
 STACK_SHAPE_SHARED = dict(d=4096, f=3001, r=256)
 # fewer neurons than SMs: most CTAs own one neuron (a one-row logit tile) or none
@@ -304,7 +303,7 @@ def _stack_vs_oracle(P, w, layers, X, ffn, tag, hot_prefix=0):
 
 
 @pytest.mark.parametrize("shape", [STACK_SHAPE, STACK_SHAPE_TC, STACK_SHAPE_SHARED, STACK_SHAPE_FEW],
-                         ids=["r136", "r144", "d4096", "f100"])
+                         ids=["r136", "r160", "d4096", "f100"])
 @pytest.mark.parametrize("wi", range(5))
 def test_decode_stack_both_paths_batch1(P, wi, shape):
     """Batch 1: the single persistent kernel and the multi-kernel step both match the oracle."""
@@ -430,8 +429,9 @@ P2_WIDE_SHAPE = dict(d=1024, f=30000, r=1024)
 @pytest.mark.parametrize("wi,shape", [(wi, STACK_SHAPE) for wi in range(5)] + [(1, P2_WIDE_SHAPE), (3, P2_WIDE_SHAPE)])
 def test_decode_stack_p2_staging_bit_identical(P, wi, shape):
     """Copying the next layer's owned P2 rows into shared memory ahead of their logits (all of
-    them, or the first ones when they do not all fit) changes nothing in the output bits (these
-    shapes keep the logits on the CUDA cores: r % 16 != 0, or not every row fits)."""
+    them, or the first ones when they do not all fit) changes nothing in the output bits: the
+    logits read the same values in the same order from either place (CUDA-core logits at
+    r = 136, tensor-core logits at r = 1024)."""
     w = _wl(wi, shape, n_layers=3)
     layers = build_layers(w, range(w.n_layers))
     X = make_inputs(w, 2, 1, seed=13, device="cpu").numpy()
