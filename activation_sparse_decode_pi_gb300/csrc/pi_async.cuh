@@ -76,6 +76,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
     return true;
 }
 
+// ---------------------------------------------------------------- named barriers -------------
+
+// Barrier `id` (1..15; 0 is __syncthreads) over `count` threads (a multiple of 32).
+__device__ __forceinline__ void bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// bar_sync that also returns the AND of v over the participating threads.
+__device__ __forceinline__ bool bar_and(int id, int count, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------- bulk copies ----------------
 
 // global -> shared, `bytes` (multiple of 16, both addresses 16-byte aligned); completion

@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     __shared__ uint64_t s_p2bar[STACK_P2_TILES];   // P2 tile slot j: its rows have landed
     __shared__ int s_p2use[STACK_P2_TILES];        // tiles slot j holds per layer
     __shared__ int s_p2par[STACK_P2_TILES];        // parity of slot j's copies in flight across a grid barrier (-1: none)
+    __shared__ int s_p2iss[STACK_P2_TILES];        // uses of slot j issued in the current layer's logits
     __shared__ float spb[STACK_MAX_CHUNK];   // predictor bias of the owned rows, copied during phase A
     __shared__ const void *s_p2next;          // P2 of the next layer (read during phase A)
     __shared__ int s_pend;         // parity of the last hot-slot copies issued (-1: none)
@@ -259,11 +260,13 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
         const int lo = max(16 * t, ks0), hi = min(16 * t + 16, K);
         return hi > lo ? (uint32_t)((hi - lo) * p2b) : 0u;
     };
-    // parity of the phase of slot t % RT that holds tile t of layer l
+    // parity of the phase of slot t % RT that holds tile t of layer l (timeout paths only: it divides)
     auto tile_par = [&](int l, int t) -> uint32_t {
         const int j = t % RT;
         return (uint32_t)(l * s_p2use[j] + t / RT) & 1u;
     };
+    // the same for one of the first RT tiles (slot t, first use in the layer)
+    auto tile_par0 = [&](int l, int t) -> uint32_t { return (uint32_t)(l * s_p2use[t]) & 1u; };
     // copy rows [lo, hi) of tile t (owned rows) into its slot; the ring there is free
     auto copy_tile_rows = [&](const void *p2, int t, int j, int lo, int hi) {
         for (int k = max(lo, ks0); k < hi && k < K; ++k) {
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     auto expect_p2 = [&](int l) {
         if (tid < NI) {
             mbar_arrive_expect_tx(&s_p2bar[tid], tile_bytes(tid));
-            s_p2par[tid] = (int)tile_par(l, tid);
+            s_p2par[tid] = (int)tile_par0(l, tid);
         }
     };
     // one copy per thread, row k = 16 * lane + warp (a warp's copies are issued one after another,
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             // the CTA leaves once its copies in flight have landed
             auto wait_staged = [&](int nt) -> bool {
                 bool ok = true;
-                for (int j = 0; j < nt; ++j) ok = mbar_wait(&s_p2bar[j], tile_par(l, j)) && ok;
+                for (int j = 0; j < nt; ++j) ok = mbar_wait(&s_p2bar[j], tile_par0(l, j)) && ok;
                 if (__syncthreads_and(ok)) return true;
                 if (tid == 0) {
                     set_status(a.status, ST_TIMEOUT);
@@ -578,45 +581,60 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                         act = c + P * tid < a.hot_prefix || z > a.tau;
                     }
                 } else {
-                    // more tiles than slots: tile by tile, every warp taking a 1/16 share of its k
-                    // steps; the slot is refilled with the tile RT further on once the tile's products
-                    // are done, so up to RT - 1 tiles of copies stay in flight
+                    // More tiles than slots: two groups of 8 warps take the tiles in turn (group g:
+                    // tiles g, g + 2, ...), each warp of a group a 1/8 share of a tile's k steps, with
+                    // a named barrier per group, so one group's synchronisation overlaps the other's
+                    // products. A slot is refilled with the tile RT further on as soon as its tile's
+                    // products are done (the mbarrier hands it to whichever group takes that tile),
+                    // so up to RT - 2 tiles of copies stay in flight.
                     float *zt = sbias;   // the tiles' logits (sbias is written only after the list)
-                    const int s0 = warp * NKS / SNW, s1 = (warp + 1) * NKS / SNW;
-                    int j = 0, wrap = 0;   // slot of tile t, and t / RT
-                    for (int t = 0; t < MT; ++t) {
-                        const bool ok = mbar_wait(&s_p2bar[j], (uint32_t)(l * s_p2use[j] + wrap) & 1u);
-                        if (!__syncthreads_and(ok)) {
-                            if (tid == 0) {
-                                set_status(a.status, ST_TIMEOUT);
-                                drain_tiles(l, t, t + RT);
-                            }
-                            return;
-                        }
+                    const int grp = warp >> 3, gw = warp & 7, gtid = tid & 255;
+                    const int s0 = gw * NKS / 8, s1 = (gw + 1) * NKS / 8;
+                    if (tid < RT) s_p2iss[tid] = tid < NI ? 1 : 0;   // uses of each slot issued in this layer
+                    __syncthreads();
+                    bool ok = true;
+                    int j = grp, wrap = 0;   // slot of tile t, and t / RT (RT >= 2)
+                    for (int t = grp; t < MT; t += 2) {
+                        ok = mbar_wait(&s_p2bar[j], (uint32_t)(l * s_p2use[j] + wrap) & 1u);
+                        ok = bar_and(1 + grp, 256, ok);   // the group decides together
+                        if (!ok) break;
                         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                         tile_mma(t, j, s0, s1, acc);
-                        float *zb = zp + (t & 1) * (SNW * 16);   // double-buffered partials
+                        float *zb = zp + ((grp * 2 + ((t >> 1) & 1)) * 8) * 16;   // per group, double-buffered
                         if ((lane & 3) == 0) {
-                            zb[warp * 16 + (lane >> 2)] = (acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1]);
-                            zb[warp * 16 + (lane >> 2) + 8] = (acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3]);
+                            zb[gw * 16 + (lane >> 2)] = (acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1]);
+                            zb[gw * 16 + (lane >> 2) + 8] = (acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3]);
                         }
-                        __syncthreads();   // the slot's rows are read and the partials written
-                        if (tid < 16) {
+                        bar_sync(1 + grp, 256);   // the slot's rows are read and the partials written
+                        if (gtid < 16) {
                             float z = 0.f;
-                            for (int w = 0; w < SNW; ++w) z += zb[w * 16 + tid];   // fixed order
-                            zt[t * 16 + tid] = z;
+                            for (int w = 0; w < 8; ++w) z += zb[w * 16 + gtid];   // fixed order
+                            zt[t * 16 + gtid] = z;
                         }
                         const int tn = t + RT;
                         if (tn < MT) {   // refill: one thread registers the bytes, 16 threads copy a row each
-                            if (tid == 32) mbar_arrive_expect_tx(&s_p2bar[j], tile_bytes(tn));
-                            if (tid >= 64 && tid < 80) copy_tile_rows(Lw.p2, tn, j, tn * 16 + tid - 64, tn * 16 + tid - 63);
+                            if (gtid == 32) {
+                                s_p2iss[j] += 1;
+                                mbar_arrive_expect_tx(&s_p2bar[j], tile_bytes(tn));
+                            }
+                            if (gtid >= 64 && gtid < 80)
+                                copy_tile_rows(Lw.p2, tn, j, tn * 16 + gtid - 64, tn * 16 + gtid - 63);
                         }
-                        if (++j == RT) {
-                            j = 0;
+                        j += 2;
+                        if (j >= RT) {
+                            j -= RT;
                             ++wrap;
                         }
                     }
-                    __syncthreads();
+                    if (!__syncthreads_and(ok)) {
+                        // a group gave up: wait (bounded) for every slot's last copies, then leave
+                        if (tid == 0) {
+                            set_status(a.status, ST_TIMEOUT);
+                            for (int q = 0; q < RT; ++q)
+                                if (s_p2iss[q] > 0) mbar_wait(&s_p2bar[q], (uint32_t)(l * s_p2use[q] + s_p2iss[q] - 1) & 1u);
+                        }
+                        return;
+                    }
                     if (tid < K) {
                         const float z = zt[tid] + spb[tid];
                         act = c + P * tid < a.hot_prefix || z > a.tau;
