@@ -186,7 +186,7 @@ struct pi_ffn {
     int stack_slots = 0, stack_slot_bytes = 0;
     size_t stack_smem = 0;
     unsigned long long *phase_stamps = nullptr;   // pi_ffn_set_phase_trace (borrowed device buffer)
-    int stack_pf = 0;                  // next-layer L2 prefetch of the persistent step (PI_FFN_STACK_PF)
+    int stack_pf = 1;                  // L2 prefetch of the persistent step: bit 0 P1, bit 1 unstaged P2 rows (PI_FFN_STACK_PF)
     int off_ring = 0, off_flags = 0, off_mbar = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
     // tensor-core path (batch >= tc_min_b)
     bool tc_ok = false;
@@ -651,13 +651,14 @@ void plan_stack(pi_ffn_t *h)
     if (!(p2env && p2env[0] == '0') && p2row % 16 == 0)
         h->stack_p2 = (int)std::min({(size_t)STACK_P2_TILES, ring / (16 * p2st), (own + 15) / 16});
     h->stack_smem = off_ring + std::max((size_t)h->stack_ring, (size_t)h->stack_p2 * 16 * p2st);
-    // The next layer's predictor rows are prefetched into L2 a layer ahead only while one layer's
-    // predictor is small next to L2 (129 MB): a larger one is evicted by the layer's own traffic
-    // before it is read, and the prefetch then costs its bytes twice (measured on the OPT-175B
-    // shape: 1.31x the algorithmic DRAM bytes, 13% slower).
+    // The next layer's P1 rows go to L2 during the grid barrier after the FFN (they land during the
+    // reduction, just before the predictor reads them). The P2 rows that are not staged go to L2 a
+    // whole layer ahead only while one layer's predictor is small next to L2 (129 MB): a larger
+    // one is evicted by the layer's own traffic before it is read, and the prefetch then costs its
+    // bytes twice (measured on the OPT-175B shape: 1.31x the algorithmic DRAM bytes, 13% slower).
     const size_t pred_bytes = elt_row_bytes(D.pdtype, D.d) * D.r + p2row * D.f;
-    h->stack_pf = pred_bytes <= (40u << 20) ? 2 : 0;
-    if (const char *pf = std::getenv("PI_FFN_STACK_PF")) h->stack_pf = std::max(0, std::min(2, std::atoi(pf)));
+    h->stack_pf = 1 | (pred_bytes <= (40u << 20) ? 2 : 0);
+    if (const char *pf = std::getenv("PI_FFN_STACK_PF")) h->stack_pf = std::max(0, std::min(3, std::atoi(pf)));
     h->stack_ok = true;
 }
 
@@ -700,7 +701,8 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.hot_k = h->n_hot > 0 ? std::min((h->n_hot + h->nsm - 1) / h->nsm, h->stack_slots - 2) : 0;
     if (a.hot_k < 0) a.hot_k = 0;
     a.p2_tiles = a.hot_k > 0 ? 0 : h->stack_p2;   // the hot slots hold the ring between layers
-    a.pf = h->stack_pf;
+    a.pf_p1 = h->stack_pf & 1;
+    a.pf_p2 = (h->stack_pf >> 1) & 1;
     a.x_layers = x_layers;
     a.stamps = h->phase_stamps;
     a.bias_bulk = D.f % 4 == 0 ? 1 : 0;

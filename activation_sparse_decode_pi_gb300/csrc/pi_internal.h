@@ -86,7 +86,8 @@ struct StackArgs {
     int hot_k;                    // ring slots per CTA held by hot owned neurons (loaded a layer ahead), <= slots - 2
     int hot_prefix;               // neurons below this are active without a logit
     int p2_tiles;                 // ring slots for 16-row tiles of owned P2 rows (0: none)
-    int pf;                       // next-layer L2 prefetch: 0 none, 1 P1 rows, 2 P1 and the unstaged P2 rows
+    int pf_p1;                    // the next layer's P1 rows into L2 during the grid barrier after the FFN
+    int pf_p2;                    // the next layer's unstaged P2 rows into L2 a layer ahead
     float *x_layers;              // optional [L x d]: row l = x_{l+1} (every layer's output), or NULL
     unsigned long long *stamps;   // optional [L x STACK_PHASES x grid] %globaltimer stamps, or NULL
 };

@@ -314,13 +314,17 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     const int nchp = d / VP;
     const int pa_per = (nchp + SNW - 1) / SNW, pa_cb = warp * pa_per, pa_ce = min(nchp, pa_cb + pa_per);
     RowChunks<PT, 8, 1> pa;
-    // the rest of this CTA's predictor slice, into L2
-    // (one prefetch per thread: thread k in [KS, K) takes owned P2 row k, the last thread the P1 rows)
-    auto prefetch_predictor = [&](const StackLayer &L) {
-        if (a.pf >= 2 && tid >= KS && tid < K)
-            prefetch_l2((const char *)L.p2 + (size_t)(c + (size_t)P * tid) * r * pb, r * pb);
-        if (a.pf >= 1 && tid == STACK_NT - 1)
+    // This CTA's P1 rows of a layer into L2 (the last thread), issued inside the grid barrier that
+    // follows the previous layer's FFN, so that they land during the reduction phase.
+    auto prefetch_p1 = [&](const StackLayer &L) {
+        if (a.pf_p1 && tid == STACK_NT - 1)
             prefetch_l2_range((const char *)L.p1 + (size_t)k0 * d * pb, (size_t)(k1 - k0) * d * pb);
+    };
+    // The owned P2 rows that are not staged, into L2 a whole layer ahead (one row per thread):
+    // only while a layer's predictor is small next to L2.
+    auto prefetch_p2 = [&](const StackLayer &L) {
+        if (a.pf_p2 && tid >= KS && tid < K)
+            prefetch_l2((const char *)L.p2 + (size_t)(c + (size_t)P * tid) * r * pb, r * pb);
     };
 
     // the hot owned neurons of layer Lw into their slots, one issuing thread per neuron; the
@@ -352,7 +356,8 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     }
     __syncthreads();   // the barriers are initialised and s_p2use is set
     expect_p2(0);
-    prefetch_predictor(a.layers[0]);
+    prefetch_p1(a.layers[0]);
+    prefetch_p2(a.layers[0]);
     __syncthreads();
     issue_hot(a.layers[0], -1);
     if (KS > 0) stage_p2(a.layers[0].p2);
@@ -414,7 +419,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 ssq = warp_sum(ssq);
                 if (lane == 0) s_inv = 1.0f / sqrtf(ssq / (float)d + a.eps);
             }
-            if (l + 1 < a.L) prefetch_predictor(a.layers[l + 1]);
+            if (l + 1 < a.L) prefetch_p2(a.layers[l + 1]);
             const uint4 *row[8];
             const __half *srow[8];
 #pragma unroll
@@ -771,44 +776,74 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 float v[NV];   // gated: gate and up partial of neuron k at 2k, 2k + 1; else gate at k
 #pragma unroll
                 for (int j = 0; j < NV; ++j) v[j] = 0.f;
+                // the batch's slots land first; then every thread walks its columns of all the batch's
+                // rows at once, one dependent chain per neuron and row, the chains interleaved (each
+                // neuron's additions keep their order: the same bits as one neuron at a time)
+                const unsigned char *sls[NB];
 #pragma unroll
                 for (int k = 0; k < NB; ++k) {
-                    if (k >= mb) break;
-                    uint32_t par;
-                    const int slot = slot_at(m0, cold, k, par);
-                    const unsigned char *sl = ring + (size_t)slot * a.slot_bytes;
-                    got = got && mbar_wait(&mbar[slot], par);
-                    if (!got) continue;
+                    sls[k] = sls[0];   // an unused neuron reads the first neuron's (landed) slot; its sums are never used
+                    if (k < mb) {
+                        uint32_t par;
+                        const int slot = slot_at(m0, cold, k, par);
+                        sls[k] = ring + (size_t)slot * a.slot_bytes;
+                        got = got && mbar_wait(&mbar[slot], par);
+                    }
+                }
+                if (got) {
                     constexpr int GI = KIND == KIND_GATED ? 2 : 1;
 #pragma unroll
                     for (int cc = 0; cc < CPT; ++cc) {
                         const int ci = tid + cc * STACK_NT;
                         if (ci >= nchw) break;
-                        const uint4 wg = reinterpret_cast<const uint4 *>(sl)[ci];
                         if constexpr (WT == DT_INT4) {
-                            const __half *ss = reinterpret_cast<const __half *>(sl + ROWS * rowb);
-                            const uint32_t ag[4] = {wg.x, wg.y, wg.z, wg.w};
-                            float tg = 0.f;
+                            uint32_t ag[NB][4];
+                            float tg[NB];
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) tg = fmaf(nib(ag[e >> 3], e & 7), ur[cc][e], tg);
-                            v[GI * k] = fmaf(__half2float(ss[ci >> 2]), tg, v[GI * k]);
-                            if (KIND == KIND_GATED) {
-                                const uint4 wu = reinterpret_cast<const uint4 *>(sl + rowb)[ci];
-                                const uint32_t au[4] = {wu.x, wu.y, wu.z, wu.w};
-                                float tu = 0.f;
+                            for (int k = 0; k < NB; ++k) {
+                                const uint4 w = reinterpret_cast<const uint4 *>(sls[k])[ci];
+                                ag[k][0] = w.x; ag[k][1] = w.y; ag[k][2] = w.z; ag[k][3] = w.w;
+                                tg[k] = 0.f;
+                            }
 #pragma unroll
-                                for (int e = 0; e < 32; ++e) tu = fmaf(nib(au[e >> 3], e & 7), ur[cc][e], tu);
-                                v[GI * k + 1] = fmaf(__half2float(ss[d / 128 + (ci >> 2)]), tu, v[GI * k + 1]);
+                            for (int e = 0; e < 32; ++e)
+#pragma unroll
+                                for (int k = 0; k < NB; ++k) tg[k] = fmaf(nib(ag[k][e >> 3], e & 7), ur[cc][e], tg[k]);
+#pragma unroll
+                            for (int k = 0; k < NB; ++k) {
+                                const __half *ss = reinterpret_cast<const __half *>(sls[k] + ROWS * rowb);
+                                v[GI * k] = fmaf(__half2float(ss[ci >> 2]), tg[k], v[GI * k]);
+                            }
+                            if constexpr (KIND == KIND_GATED) {
+#pragma unroll
+                                for (int k = 0; k < NB; ++k) {
+                                    const uint4 w = reinterpret_cast<const uint4 *>(sls[k] + rowb)[ci];
+                                    ag[k][0] = w.x; ag[k][1] = w.y; ag[k][2] = w.z; ag[k][3] = w.w;
+                                    tg[k] = 0.f;
+                                }
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+#pragma unroll
+                                    for (int k = 0; k < NB; ++k)
+                                        tg[k] = fmaf(nib(ag[k][e >> 3], e & 7), ur[cc][e], tg[k]);
+#pragma unroll
+                                for (int k = 0; k < NB; ++k) {
+                                    const __half *ss = reinterpret_cast<const __half *>(sls[k] + ROWS * rowb);
+                                    v[GI * k + 1] = fmaf(__half2float(ss[d / 128 + (ci >> 2)]), tg[k], v[GI * k + 1]);
+                                }
                             }
                         } else {
-                            float wf[VW];
-                            unpack<WT>(wg, wf);
 #pragma unroll
-                            for (int e = 0; e < VW; ++e) v[GI * k] = fmaf(wf[e], ur[cc][e], v[GI * k]);
-                            if (KIND == KIND_GATED) {
-                                unpack<WT>(reinterpret_cast<const uint4 *>(sl + rowb)[ci], wf);
+                            for (int g = 0; g < GI; ++g) {   // gate rows, then up rows
+                                float wf[NB][VW];
 #pragma unroll
-                                for (int e = 0; e < VW; ++e) v[GI * k + 1] = fmaf(wf[e], ur[cc][e], v[GI * k + 1]);
+                                for (int k = 0; k < NB; ++k)
+                                    unpack<WT>(reinterpret_cast<const uint4 *>(sls[k] + g * rowb)[ci], wf[k]);
+#pragma unroll
+                                for (int e = 0; e < VW; ++e)
+#pragma unroll
+                                    for (int k = 0; k < NB; ++k)
+                                        v[GI * k + g] = fmaf(wf[k][e], ur[cc][e], v[GI * k + g]);
                             }
                         }
                     }
@@ -904,6 +939,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             if (tid == 0 && a.hot_k > 0) s_pend = (l + 1) & 1;
         }
         if (!sync_grid([&] {
+                if (l + 1 < a.L) prefetch_p1(a.layers[l + 1]);
                 if (l + 1 < a.L && a.hot_k > 0) issue_hot(a.layers[l + 1], l);
                 if (l + 1 < a.L && KS > 0) stage_p2(s_p2next);
             }))

@@ -33,8 +33,12 @@
  * Environment, read at pi_ffn_create (all optional; the defaults are the tuned paths):
  *  - PI_FFN_STACK_KERNEL=0  batch-1 steps use the multi-kernel chain instead of the
  *                           persistent one-kernel step.
- *  - PI_FFN_STACK_P2=0      the persistent step reads the predictor's P2 rows from L2
- *                           instead of staging them in shared memory.
+ *  - PI_FFN_STACK_P2=0      the persistent step reads the predictor's P2 rows from memory
+ *                           instead of passing them through its shared-memory ring.
+ *  - PI_FFN_STACK_PF=n      L2 prefetches of the persistent step, a bit mask: 1 = the next
+ *                           layer's P1 rows during the grid barrier after the FFN, 2 = the next
+ *                           layer's P2 rows that the ring does not hold, a whole layer ahead.
+ *                           Default 3 while one layer's predictor is at most 40 MB, else 1.
  *  - PI_FFN_TC=0            batch >= 16 stays on the CUDA-core kernels.
  *  - PI_FFN_TC_MIN_BATCH=n  smallest batch for the tensor-core path (default 16).
  *  - PI_FFN_TC_KW, PI_FFN_TC_DS, PI_FFN_TC_STAGES, PI_FFN_TC_HIDDEN_CPT: tensor-core step
@@ -167,7 +171,7 @@ pi_status_t pi_sparse_ffn(pi_ffn_t *h, int32_t layer, const float *u, int32_t B,
  * one per CTA, so the output bits depend on the SM count (and nothing else).
  * PI_FFN_STACK_KERNEL=0 in the environment at pi_ffn_create turns it off;
  * PI_FFN_STACK_P2=0 keeps the predictor's P2 rows out of its shared memory (the logits
- * then run on the CUDA cores from L2). Other steps
+ * then run on the CUDA cores from memory). Other steps
  * run as a chain of kernels, recorded once outside stream capture into a CUDA graph
  * per (B, pointer set) and replayed.
  */
