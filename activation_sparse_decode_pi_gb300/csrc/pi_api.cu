@@ -186,6 +186,9 @@ struct pi_ffn {
     int stack_slots = 0, stack_slot_bytes = 0;
     size_t stack_smem = 0;
     unsigned long long *phase_stamps = nullptr;   // pi_ffn_set_phase_trace (borrowed device buffer)
+    int stack_p2_stage = STACK_P2_TILES;   // P2 tiles filled between layers, at most (PI_FFN_STACK_P2_STAGE)
+    int stack_balance = 0;             // persistent step: FFN neurons spread evenly over the CTAs (PI_FFN_STACK_BALANCE)
+    int32_t *stack_glist = nullptr, *stack_gcount = nullptr;
     int stack_pf = 1;                  // L2 prefetch of the persistent step: bit 0 P1, bit 1 unstaged P2 rows (PI_FFN_STACK_PF)
     int off_ring = 0, off_flags = 0, off_mbar = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
     // tensor-core path (batch >= tc_min_b)
@@ -651,14 +654,16 @@ void plan_stack(pi_ffn_t *h)
     if (!(p2env && p2env[0] == '0') && p2row % 16 == 0)
         h->stack_p2 = (int)std::min({(size_t)STACK_P2_TILES, ring / (16 * p2st), (own + 15) / 16});
     h->stack_smem = off_ring + std::max((size_t)h->stack_ring, (size_t)h->stack_p2 * 16 * p2st);
-    // The next layer's P1 rows go to L2 during the grid barrier after the FFN (they land during the
-    // reduction, just before the predictor reads them). The P2 rows that are not staged go to L2 a
-    // whole layer ahead only while one layer's predictor is small next to L2 (129 MB): a larger
-    // one is evicted by the layer's own traffic before it is read, and the prefetch then costs its
-    // bytes twice (measured on the OPT-175B shape: 1.31x the algorithmic DRAM bytes, 13% slower).
+    // While one layer's predictor is small next to L2 (129 MB), the next layer's P1 rows and the P2
+    // rows that the ring does not hold go to L2 a whole layer ahead. A larger predictor would be
+    // evicted by the layer's own traffic before it is read (measured on the OPT-175B shape: 1.31x
+    // the algorithmic DRAM bytes, 13% slower), so only its P1 rows go, during the grid barrier
+    // after the FFN, landing during the reduction just before the predictor reads them.
     const size_t pred_bytes = elt_row_bytes(D.pdtype, D.d) * D.r + p2row * D.f;
-    h->stack_pf = 1 | (pred_bytes <= (40u << 20) ? 2 : 0);
-    if (const char *pf = std::getenv("PI_FFN_STACK_PF")) h->stack_pf = std::max(0, std::min(3, std::atoi(pf)));
+    h->stack_pf = pred_bytes <= (40u << 20) ? 7 : 1;
+    if (const char *pf = std::getenv("PI_FFN_STACK_PF")) h->stack_pf = std::max(0, std::min(7, std::atoi(pf)));
+    if (const char *bl = std::getenv("PI_FFN_STACK_BALANCE")) h->stack_balance = bl[0] == '0' ? 0 : 1;
+    if (const char *ps = std::getenv("PI_FFN_STACK_P2_STAGE")) h->stack_p2_stage = std::max(0, std::atoi(ps));
     h->stack_ok = true;
 }
 
@@ -701,8 +706,12 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.hot_k = h->n_hot > 0 ? std::min((h->n_hot + h->nsm - 1) / h->nsm, h->stack_slots - 2) : 0;
     if (a.hot_k < 0) a.hot_k = 0;
     a.p2_tiles = a.hot_k > 0 ? 0 : h->stack_p2;   // the hot slots hold the ring between layers
-    a.pf_p1 = h->stack_pf & 1;
+    a.p2_stage_tiles = h->stack_p2_stage;
+    a.pf_p1 = (h->stack_pf & 4) ? 2 : (h->stack_pf & 1);   // 2: a layer ahead, 1: just in time
     a.pf_p2 = (h->stack_pf >> 1) & 1;
+    a.balance = h->stack_balance && a.hot_k == 0 ? 1 : 0;
+    a.glist = h->stack_glist;
+    a.gcount = h->stack_gcount;
     a.x_layers = x_layers;
     a.stamps = h->phase_stamps;
     a.bias_bulk = D.f % 4 == 0 ? 1 : 0;
@@ -787,6 +796,8 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
         tnb * h->tc_fpad * 2, tnb * h->tc_fpad * 2,    // tc_hhi, tc_hlo
         (size_t)h->nsm * 2 * 256 * 128 * 4 * (tnb ? 1 : 0),   // tc_part: two slots of up to 256 accumulator columns
         h->tc_ok ? (size_t)(h->tc_ntiles + 1) * 4 : 0, // tc_cnt
+        (size_t)h->nsm * STACK_MAX_CHUNK * 4,          // stack_glist
+        (size_t)h->nsm * 4,                            // stack_gcount
     };
     const int nbuf = sizeof(sizes) / sizeof(sizes[0]);
     size_t off[32], total = 0;
@@ -831,6 +842,8 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
         h->tc_part = (float *)(base + off[22]);
         h->tc_cnt = (uint32_t *)(base + off[23]);
     }
+    h->stack_glist = (int32_t *)(base + off[24]);
+    h->stack_gcount = (int32_t *)(base + off[25]);
     {
         std::vector<StackLayer> sl(D.n_layers);
         for (int l = 0; l < D.n_layers; ++l) {

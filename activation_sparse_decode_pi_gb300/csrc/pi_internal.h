@@ -86,8 +86,11 @@ struct StackArgs {
     int hot_k;                    // ring slots per CTA held by hot owned neurons (loaded a layer ahead), <= slots - 2
     int hot_prefix;               // neurons below this are active without a logit
     int p2_tiles;                 // ring slots for 16-row tiles of owned P2 rows (0: none)
-    int pf_p1;                    // the next layer's P1 rows into L2 during the grid barrier after the FFN
+    int p2_stage_tiles;           // of which filled between layers, at most (the rest as the logits start)
+    int pf_p1;                    // the next layer's P1 rows into L2: 1 during the grid barrier after the FFN, 2 a layer ahead
     int pf_p2;                    // the next layer's unstaged P2 rows into L2 a layer ahead
+    int balance;                  // spread the FFN's neurons evenly over the CTAs (one more grid barrier per layer)
+    int32_t *glist, *gcount;      // [grid x STACK_MAX_CHUNK] published lists, [grid] their counts
     float *x_layers;              // optional [L x d]: row l = x_{l+1} (every layer's output), or NULL
     unsigned long long *stamps;   // optional [L x STACK_PHASES x grid] %globaltimer stamps, or NULL
 };

@@ -251,9 +251,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     const int MT = (K + 15) >> 4, RT = a.p2_tiles;
     bool TCL = false;   // logits on the tensor cores
     if constexpr (PT == DT_BF16 || PT == DT_F16) TCL = K > 0 && (r & 15) == 0 && (MT <= RT || RT >= 2);
-    const int NI = min(MT, RT);
-    const int MTS = TCL ? MT : NI;                           // tiles through the ring per layer
-    const int KS = min(K, NI * 16);                          // rows staged between layers
+    const int NR = min(MT, RT);                              // tiles in the ring at the start of the logits
+    const int NI = min(NR, a.p2_stage_tiles);                // of which staged between layers
+    const int MTS = TCL ? MT : NR;                           // tiles through the ring per layer
+    const int KS = min(K, NR * 16);                          // rows in the ring at the start of the logits
     const int ks0 = a.hot_prefix > c ? min(K, (a.hot_prefix - c + P - 1) / P) : 0;
     // bytes of tile t's rows that are copied (past K and below the hot prefix: none)
     auto tile_bytes = [&](int t) -> uint32_t {
@@ -303,7 +304,14 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     // so every warp takes a few); the ring is free and expect_p2 ran
     auto stage_p2 = [&](const void *p2) {
         const int k = lane * SNW + warp;
-        if (k < KS) copy_tile_rows(p2, k >> 4, k >> 4, k, k + 1);   // tile k / 16 < NI sits in slot k / 16
+        if (k < min(KS, NI * 16)) copy_tile_rows(p2, k >> 4, k >> 4, k, k + 1);   // tile k / 16 < NI sits in slot k / 16
+    };
+    // tiles [NI, NR) of layer l, not staged between layers, requested as the logits start
+    // (thread 32 registers the bytes, one copy per thread)
+    auto issue_rest = [&](const StackLayer &Lw, int l) {
+        if (tid >= 32 + NI && tid < 32 + NR) mbar_arrive_expect_tx(&s_p2bar[tid - 32], tile_bytes(tid - 32));
+        const int k = lane * SNW + warp + NI * 16;
+        if (k < KS) copy_tile_rows(Lw.p2, k >> 4, k >> 4, k, k + 1);
     };
     // after a timeout: wait (bounded) for the copies of tiles [t0, t1) of layer l
     auto drain_tiles = [&](int l, int t0, int t1) {
@@ -317,7 +325,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     // This CTA's P1 rows of a layer into L2 (the last thread), issued inside the grid barrier that
     // follows the previous layer's FFN, so that they land during the reduction phase.
     auto prefetch_p1 = [&](const StackLayer &L) {
-        if (a.pf_p1 && tid == STACK_NT - 1)
+        if (tid == STACK_NT - 1)
             prefetch_l2_range((const char *)L.p1 + (size_t)k0 * d * pb, (size_t)(k1 - k0) * d * pb);
     };
     // The owned P2 rows that are not staged, into L2 a whole layer ahead (one row per thread):
@@ -348,7 +356,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
         for (int j = 0; j < RT && j < STACK_P2_TILES; ++j) mbar_init(&s_p2bar[j], 1);
         fence_mbar_init();
         s_pend = a.hot_k > 0 ? 0 : -1;
-        s_base = barrier_base(a.bar, (unsigned long long)(3 * a.L) * a.nblocks);
+        s_base = barrier_base(a.bar, (unsigned long long)((3 + (a.balance ? 1 : 0)) * a.L) * a.nblocks);
     }
     if (tid < STACK_P2_TILES) {
         s_p2use[tid] = tid < min(MTS, RT) ? (MTS - tid + RT - 1) / RT : 0;
@@ -356,7 +364,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     }
     __syncthreads();   // the barriers are initialised and s_p2use is set
     expect_p2(0);
-    prefetch_p1(a.layers[0]);
+    if (a.pf_p1) prefetch_p1(a.layers[0]);
     prefetch_p2(a.layers[0]);
     __syncthreads();
     issue_hot(a.layers[0], -1);
@@ -420,6 +428,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 if (lane == 0) s_inv = 1.0f / sqrtf(ssq / (float)d + a.eps);
             }
             if (l + 1 < a.L) prefetch_p2(a.layers[l + 1]);
+            if (l + 1 < a.L && a.pf_p1 == 2) prefetch_p1(a.layers[l + 1]);   // a whole layer ahead
             const uint4 *row[8];
             const __half *srow[8];
 #pragma unroll
@@ -501,6 +510,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                         rc.w[q][i] = ci < nchr && row[q] != nullptr ? row[q][ci] : make_uint4(0u, 0u, 0u, 0u);
                 }
             };
+            if (NI < NR) {   // the tiles not staged between layers are requested first
+                fence_proxy_async_smem();
+                issue_rest(Lw, l);
+            }
             // hp is requested first, so its reads (L2 hits) do not queue behind the P2 rows
             const int r4 = r / 4;
             float4 hv[2];
@@ -566,7 +579,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 if (MT <= RT) {
                     // every tile was staged between layers: one pass, units (tile t, k part g), G warps
                     // sharing a tile when there are fewer tiles than warps
-                    if (!wait_staged(MT)) return;
+                    if (!wait_staged(MT)) return;   // MT == NR here
                     const int G = MT >= SNW ? 1 : SNW / MT;
                     for (int u = warp; u < MT * G; u += SNW) {
                         const int t = u / G, g = u - t * G;
@@ -595,7 +608,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     float *zt = sbias;   // the tiles' logits (sbias is written only after the list)
                     const int grp = warp >> 3, gw = warp & 7, gtid = tid & 255;
                     const int s0 = gw * NKS / 8, s1 = (gw + 1) * NKS / 8;
-                    if (tid < RT) s_p2iss[tid] = tid < NI ? 1 : 0;   // uses of each slot issued in this layer
+                    if (tid < RT) s_p2iss[tid] = tid < NR ? 1 : 0;   // uses of each slot issued in this layer
                     __syncthreads();
                     bool ok = true;
                     int j = grp, wrap = 0;   // slot of tile t, and t / RT (RT >= 2)
@@ -655,7 +668,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     const int t = tid + u * STACK_NT;
                     if (t < r4) hp4[(t % QH) * nchr + t / QH] = hv[u];   // planar layout of the row dot products
                 }
-                if (!wait_staged(NI)) return;
+                if (!wait_staged(NR)) return;
                 if (tid < NI) s_p2par[tid] = -1;
                 for (int kbase = warp; kbase < K; kbase += SNW * 5) {
                     if (kbase != warp) {
@@ -699,6 +712,50 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             }
             if (tid == 0 && a.counts && nn) atomicAdd(a.counts + l, nn);
             __syncthreads();
+            if (a.balance) {
+                // Every CTA publishes its list; after one more grid barrier each takes an equal share
+                // (positions [c N / P, (c + 1) N / P)) of the lists concatenated in CTA order, so the
+                // FFN's rows are spread evenly over the SMs whatever the per-CTA counts. The order
+                // is fixed by the lists alone, so the result stays deterministic.
+                int32_t *gl = a.glist + (size_t)c * STACK_MAX_CHUNK;
+                for (int m = tid; m < nn; m += STACK_NT) gl[m] = sneur[m];
+                if (tid == 0) a.gcount[c] = nn;
+                if (!sync_grid(no_work)) return;
+                int *pref = reinterpret_cast<int *>(spb);   // [P + 1]; the logits' biases are dead now
+                if (warp == 0) {                           // exclusive prefix of the P counts
+                    int run = 0;
+                    for (int base = 0; base < P; base += 32) {
+                        const int q = base + lane;
+                        const int v = q < P ? __ldcg(a.gcount + q) : 0;
+                        int x = v;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const int y = __shfl_up_sync(0xffffffffu, x, o);
+                            if (lane >= o) x += y;
+                        }
+                        if (q < P) pref[q] = run + x - v;
+                        run += __shfl_sync(0xffffffffu, x, 31);
+                    }
+                    if (lane == 0) pref[P] = run;
+                }
+                __syncthreads();
+                const int N = pref[P];
+                const int lo = (int)((long long)c * N / P);
+                nn = (int)((long long)(c + 1) * N / P) - lo;
+                for (int m = tid; m < nn; m += STACK_NT) {
+                    const int q = lo + m;
+                    int a0 = 0, a1 = P;   // pref[a0] <= q < pref[a1]
+                    while (a1 - a0 > 1) {
+                        const int mid = (a0 + a1) >> 1;
+                        if (pref[mid] <= q) a0 = mid;
+                        else a1 = mid;
+                    }
+                    const int i = __ldcg(a.glist + (size_t)a0 * STACK_MAX_CHUNK + (q - pref[a0]));
+                    sneur[m] = i;
+                    if (!bias_bulk) sbias[m] = Lw.bg ? __ldg(Lw.bg + i) : 0.f;
+                }
+                __syncthreads();
+            }
             stamp(l, 3);
             if (nn == 0) stamp(l, 4);
 
@@ -939,7 +996,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             if (tid == 0 && a.hot_k > 0) s_pend = (l + 1) & 1;
         }
         if (!sync_grid([&] {
-                if (l + 1 < a.L) prefetch_p1(a.layers[l + 1]);
+                if (l + 1 < a.L && a.pf_p1 == 1) prefetch_p1(a.layers[l + 1]);   // just in time
                 if (l + 1 < a.L && a.hot_k > 0) issue_hot(a.layers[l + 1], l);
                 if (l + 1 < a.L && KS > 0) stage_p2(s_p2next);
             }))

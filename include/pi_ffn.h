@@ -35,10 +35,16 @@
  *                           persistent one-kernel step.
  *  - PI_FFN_STACK_P2=0      the persistent step reads the predictor's P2 rows from memory
  *                           instead of passing them through its shared-memory ring.
+ *  - PI_FFN_STACK_BALANCE=0 the persistent step computes each CTA's own active neurons instead
+ *                           of spreading the layer's active neurons evenly over the CTAs
+ *                           (which costs one more grid barrier per layer).
  *  - PI_FFN_STACK_PF=n      L2 prefetches of the persistent step, a bit mask: 1 = the next
- *                           layer's P1 rows during the grid barrier after the FFN, 2 = the next
- *                           layer's P2 rows that the ring does not hold, a whole layer ahead.
- *                           Default 3 while one layer's predictor is at most 40 MB, else 1.
+ *                           layer's P1 rows (during the grid barrier after the FFN, or a whole
+ *                           layer ahead with 4), 2 = the next layer's P2 rows that the ring does
+ *                           not hold, a whole layer ahead. Default 7 while one layer's predictor
+ *                           is at most 40 MB, else 1.
+ *  - PI_FFN_STACK_P2_STAGE=n  at most n P2 tiles are copied into the ring between layers (the
+ *                           rest as the logits start); default all that fit.
  *  - PI_FFN_TC=0            batch >= 16 stays on the CUDA-core kernels.
  *  - PI_FFN_TC_MIN_BATCH=n  smallest batch for the tensor-core path (default 16).
  *  - PI_FFN_TC_KW, PI_FFN_TC_DS, PI_FFN_TC_STAGES, PI_FFN_TC_HIDDEN_CPT: tensor-core step
@@ -326,8 +332,10 @@ pi_status_t pi_ffn_set_hot_prefix(pi_ffn_t *h, int32_t hot_prefix);
  * [0, n_hot) fire on most tokens. The persistent batch-1 kernel of pi_decode_stack then
  * requests those neurons' rows one layer ahead, before their predictor has run, into ring
  * slots of their own (at most ring slots - 2 per SM). A hot neuron that the predictor
- * rejects costs its bytes but does not change the result: the output is bit-identical for
- * every n_hot. 0 (the default) turns this off. Other paths ignore it.
+ * rejects costs its bytes but does not change the result. With hot slots every CTA computes
+ * the FFN of its own neurons (the even spread of the neurons over the CTAs is off), and the
+ * output is bit-identical for every n_hot > 0 to the output with PI_FFN_STACK_BALANCE=0.
+ * 0 (the default) turns this off. Other paths ignore it.
  * Returns PI_ERR_INVALID_ARG unless 0 <= n_hot <= f. Takes effect from the next call.
  */
 pi_status_t pi_ffn_set_hot_neurons(pi_ffn_t *h, int32_t n_hot);

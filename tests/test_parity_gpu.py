@@ -380,11 +380,12 @@ def test_grid_barrier_gives_up_cleanly(P):
 
 @pytest.mark.parametrize("wi", range(5))
 def test_decode_stack_hot_neurons_bit_identical(P, wi):
-    """Requesting the hot neurons' rows a layer ahead changes nothing in the output bits."""
+    """Requesting the hot neurons' rows a layer ahead changes nothing in the output bits (hot slots
+    keep every CTA on its own neurons, so the comparison runs with the FFN balancing off)."""
     w = _wl(wi, STACK_SHAPE, n_layers=3)
     layers = build_layers(w, range(w.n_layers))
     X = make_inputs(w, 3, 1, seed=11, device="cpu").numpy()
-    ffn = _handle(P, w, [g for g, _ in layers], stack_kernel=True)
+    ffn = _with_env("PI_FFN_STACK_BALANCE", "0", lambda: _handle(P, w, [g for g, _ in layers], stack_kernel=True))
     ref = []
     for t in range(X.shape[0]):
         counts = torch.zeros(w.n_layers, dtype=torch.int32, device="cuda")
