@@ -101,30 +101,6 @@ __device__ __forceinline__ float nib(uint32_t w, int k)
     return (float)((int32_t)(w << (28 - 4 * k)) >> 28);
 }
 
-// int4 without an integer-to-float conversion. Nibble k of a 32-bit word sits at position
-// pos(k) = k (k < 5) of the word, or k - 5 of the word shifted right by 20 (k >= 5). Made
-// offset-binary (XOR 8) and OR-ed into the mantissa of 2^23 at bit 4 * pos, it reads as the
-// float 2^23 + (q + 8) * 16^pos; subtracting 2^23 + 8 * 16^pos leaves 16^pos * q exactly (every
-// value is an integer below 2^24). A factor pre-multiplied by 16^-pos (exact: a power of two)
-// then gives the same fp32 product as q times the factor.
-__host__ __device__ constexpr int nib_pos(int k) { return k < 5 ? k : k - 5; }
-
-template <int K>
-__device__ __forceinline__ float nib_scaled(uint32_t w, uint32_t w20)
-{
-    constexpr int pos = nib_pos(K);
-    const uint32_t src = K < 5 ? w : w20;
-    const uint32_t bits = (src & (0xFu << (4 * pos))) ^ (0x4B000000u | (8u << (4 * pos)));
-    return __uint_as_float(bits) - (8388608.0f + 8.0f * (float)(1u << (4 * pos)));
-}
-
-// 16^-pos(k) for element k of a 32-bit int4 word
-__host__ __device__ constexpr float nib_unscale(int k)
-{
-    return nib_pos(k) == 0 ? 1.0f : nib_pos(k) == 1 ? 0.0625f : nib_pos(k) == 2 ? 0.00390625f
-                                  : nib_pos(k) == 3 ? 0.000244140625f : 0.0000152587890625f;
-}
-
 template <>
 __device__ __forceinline__ void unpack<DT_INT4>(const uint4 &w, float (&o)[32])
 {

@@ -46,19 +46,19 @@ DEFAULT_WORKLOAD = "opt175b_d12288_f49152_int4_L96"
 CSRC = os.path.join(ROOT, "activation_sparse_decode_pi_gb300", "csrc")
 
 # DRAM traffic of the dominant kernel per launch, from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), with a hash of the kernel sources it was taken on. The capture ran a
-# 4-layer slice of the workload; traffic grows in proportion to layers, so it is kept per layer.
-# A source change makes the recorded figure stale and the bench then reports null.
-# DRAM bytes (read + write) per launch of a kernel, from one ncu capture, valid while the
-# sources that kernel is built from hash to the value recorded with it
+# dram__bytes_write.sum), valid while the sources that kernel is built from hash to the value
+# recorded with it (a source change makes the figure stale and the bench then reports null). The
+# capture ran a 4-layer slice of the workload; every layer streams the same kind of bytes, so the
+# figure is kept per layer and scaled by the layer count.
 KERNEL_SOURCES = {
     "decode_stack": ("pi_stack.cuh", "pi_stack_f32.cu", "pi_stack_bf16.cu", "pi_stack_f16.cu", "pi_stack_int4.cu",
                      "pi_async.cuh", "pi_common.cuh", "pi_rowdot.cuh", "pi_umma.cuh", "pi_internal.h"),
 }
 NCU_TRAFFIC = {
-    # 4-layer slice: dram__bytes_read.sum 234.360320 MB + dram__bytes_write.sum 3.651584 MB
-    ("relullama7b_d4096_f11008_bf16_L32", "decode_stack"): {"bytes_per_layer": (234360320 + 3651584) / 4,
-                                                            "csrc": "1b5e2ff6c00d8641"},
+    # first 4 layers: dram__bytes_read.sum + dram__bytes_write.sum, mean of two launches
+    # (608.814592 + 23.172352 MB and 613.465856 + 19.868672 MB)
+    ("opt175b_d12288_f49152_int4_L96", "decode_stack"): {
+        "bytes_per_layer": (608814592 + 23172352 + 613465856 + 19868672) / 2 / 4, "csrc": "bb41e52ed5a446db"},
 }
 
 

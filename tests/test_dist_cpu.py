@@ -76,11 +76,11 @@ def test_ncu_traffic_only_for_the_captured_configuration():
     import bench
     from workload import WORKLOADS
 
-    name = "relullama7b_d4096_f11008_bf16_L32"
+    name = "opt175b_d12288_f49152_int4_L96"
     w = WORKLOADS[name]
     rec = bench.NCU_TRAFFIC[(name, "decode_stack")]
     if rec["csrc"] == bench.csrc_hash("decode_stack"):
-        assert bench.ncu_traffic(w, "decode_stack") == pytest.approx(rec["bytes_per_layer"] * 32)
+        assert bench.ncu_traffic(w, "decode_stack") == pytest.approx(rec["bytes_per_layer"] * 96)
         assert bench.ncu_traffic(dataclasses.replace(w, n_layers=4), "decode_stack") == pytest.approx(
             rec["bytes_per_layer"] * 4)
     else:   # sources changed since the capture: no traffic figure
