@@ -191,7 +191,7 @@ struct pi_ffn {
     int32_t *stack_glist = nullptr, *stack_gcount = nullptr;
     int stack_pf = 1;                  // L2 prefetch of the persistent step: bit 0 P1, bit 1 unstaged P2 rows (PI_FFN_STACK_PF)
     int off_ring = 0, off_flags = 0, off_mbar = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
-    // tensor-core path (batch >= tc_min_b)
+    // tensor-core path (batch >= tc_min_b, set by plan_tc)
     bool tc_ok = false;
     int tc_min_b = 16, tc_nbmax = 0, tc_rpad = 0, tc_fpad = 0;
     int tc_stages[5][4][2] = {};       // [mode][log2(NB / 16)][log2(w)]
@@ -321,11 +321,16 @@ bool tc_use(const pi_ffn_t *h, int B) { return h->tc_ok && B >= h->tc_min_b && B
 
 // Whether the tensor-core kernels serve batches >= tc_min_b on this handle (16-bit weights
 // and predictor of one type, d % 128 == 0, r % 64 == 0), and their shared-memory rings.
+// The CUDA-core chain's time grows with the batch (one FMA chain per row and neuron) while
+// the tensor-core kernels cost about the same for any batch up to their 16-row tile, so
+// the crossover moves down as rows get longer: measured on a GB300 at batch 3 for d 5120
+// and d 7168 (batch 2 still faster on the chain), between batches 4 and 6 for d 4096.
 // PI_FFN_TC=0 turns the path off; PI_FFN_TC_MIN_BATCH moves its lower batch bound.
 void plan_tc(pi_ffn_t *h)
 {
     h->tc_ok = false;
     const pi_ffn_desc_t &D = h->desc;
+    h->tc_min_b = D.d >= 5120 ? 3 : 6;
     const char *env = std::getenv("PI_FFN_TC");
     if (env && env[0] == '0') return;
     if (const char *mb = std::getenv("PI_FFN_TC_MIN_BATCH")) {

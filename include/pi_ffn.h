@@ -45,8 +45,9 @@
  *                           is at most 40 MB, else 1.
  *  - PI_FFN_STACK_P2_STAGE=n  at most n P2 tiles are copied into the ring between layers (the
  *                           rest as the logits start); default all that fit.
- *  - PI_FFN_TC=0            batch >= 16 stays on the CUDA-core kernels.
- *  - PI_FFN_TC_MIN_BATCH=n  smallest batch for the tensor-core path (default 16).
+ *  - PI_FFN_TC=0            every batch > 1 stays on the CUDA-core kernels.
+ *  - PI_FFN_TC_MIN_BATCH=n  smallest batch for the tensor-core path (default 3 for
+ *                           d >= 5120, else 6).
  *  - PI_FFN_TC_KW, PI_FFN_TC_DS, PI_FFN_TC_STAGES, PI_FFN_TC_HIDDEN_CPT: tensor-core step
  *    widths (64-wide K blocks per step, 128-column W_down slices per tile: 1 or 2, default
  *    2), ring depth cap, and CTAs per predictor-hidden tile (default 8).
@@ -297,7 +298,7 @@ pi_status_t pi_sparse_ffn_noalloc(const pi_ffn_desc_t *desc, const pi_layer_weig
 pi_status_t pi_selftest_grid_barrier(uint32_t *work, int32_t extra, void *stream);
 
 /*
- * Check of the tensor-core (tcgen05) operand layouts used by the batch >= 16 path: one
+ * Check of the tensor-core (tcgen05) operand layouts used by the batched path: one
  * CTA stages A and B in shared memory the way those kernels do, multiplies them on the
  * tensor cores with an fp32 accumulator in tensor memory, and writes
  * d[128 x n] = A * B^T (row-major fp32, device).

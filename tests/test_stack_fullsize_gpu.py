@@ -6,7 +6,8 @@ of the oracle runs on the GPU's own x_l, so every layer is compared).
   column chunks per thread), OPT-30B-shaped (fp16, non-gated, d 7168; only part of each
   CTA's P2 rows fit in shared memory), OPT-175B-shaped (int4 group-128, d 12288; part of
   the P2 rows staged);
-* batch 4 runs the kernel chain, batches 16 and 32 the tensor-core kernels.
+* batch 2 runs the CUDA-core kernel chain, batches 4, 16 and 32 the tensor-core kernels
+  (their lower batch bound is 3 at these row lengths).
 A few layers of each stack are enough: every layer has the same shape and law.
 """
 import dataclasses
@@ -24,6 +25,7 @@ CASES = [
     ("llama2_13b_d5120_f13824_bf16_L40", 1, 3),
     ("opt30b_d7168_f28672_fp16_L48", 1, 3),
     ("opt175b_d12288_f49152_int4_L96", 1, 3),
+    ("llama2_13b_d5120_f13824_bf16_L40", 2, 2),
     ("llama2_13b_d5120_f13824_bf16_L40", 4, 2),
     ("llama2_13b_d5120_f13824_bf16_L40", 16, 2),
     ("opt30b_d7168_f28672_fp16_L48", 32, 2),
@@ -50,6 +52,8 @@ def test_stack_full_size_teacher_forced(P, name, B, n_layers):
         assert prof["decode_stack"][1] == 1 and prof["ffn_h"][1] == 0, prof   # the persistent kernel ran
     else:
         assert prof["decode_stack"][1] == 0 and prof["ffn_h"][1] == n_layers, prof
+        # the chain normalises once per step, the tensor-core path splits each layer's input
+        assert prof["rms"][1] == (1 if B == 2 else n_layers), prof
     flips = 0
     for t in range(X.shape[0]):
         xo = ffn.decode_stack(to_dev(X[t])).clone()

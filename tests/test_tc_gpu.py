@@ -1,4 +1,4 @@
-"""Tensor-core (tcgen05) path of the batch >= 16 kernels.
+"""Tensor-core (tcgen05) path of the batched kernels.
 
 First the operand layouts on their own: one tile product D = A * B^T through
 pi_selftest_umma, with small-integer operands so that every product and sum is
