@@ -101,6 +101,44 @@ __device__ __forceinline__ float nib(uint32_t w, int k)
     return (float)((int32_t)(w << (28 - 4 * k)) >> 28);
 }
 
+__device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c)   // (a & b) ^ c
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
+__device__ __forceinline__ __half2 u32_h2(uint32_t v) { return *reinterpret_cast<__half2 *>(&v); }
+
+// The eight signed 4-bit values of w (value e in bits [4e + 3 : 4e]) as exact fp32 pairs:
+// p[i] = (v_i, v_{i+4}), i < 4. Each 16-bit half is built as the fp16 number 1024 + (v + 8) by
+// masking a nibble into the mantissa of 1024 (flipping the nibble's top bit turns two's
+// complement into offset binary); subtracting 1032 leaves v exactly. A nibble in bits 4..7 of a
+// half lands as 16 (v + 8) and is scaled back by 1/16 in the same exact fused step. Integer to
+// float conversions are avoided: they share the integer pipe with the shifts and masks.
+__device__ __forceinline__ void i4_word_f32x2(uint32_t w, float2 (&p)[4])
+{
+    const uint32_t w8 = w >> 8;
+    const __half2 k1032 = u32_h2(0x64086408u);   // 1032
+    const __half2 k16th = u32_h2(0x2C002C00u);   // 1 / 16
+    const __half2 km72 = u32_h2(0xD480D480u);    // -72 = -(1024 / 16 + 8)
+    p[0] = __half22float2(__hsub2(u32_h2(lop3_and_xor(w, 0x000F000Fu, 0x64086408u)), k1032));
+    p[1] = __half22float2(__hfma2(u32_h2(lop3_and_xor(w, 0x00F000F0u, 0x64806480u)), k16th, km72));
+    p[2] = __half22float2(__hsub2(u32_h2(lop3_and_xor(w8, 0x000F000Fu, 0x64086408u)), k1032));
+    p[3] = __half22float2(__hfma2(u32_h2(lop3_and_xor(w8, 0x00F000F0u, 0x64806480u)), k16th, km72));
+}
+
+// (a.x b.x + c.x, a.y b.y + c.y): two fp32 FMAs in one instruction, each rounded as fmaf.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)),
+          "l"(*reinterpret_cast<unsigned long long *>(&c)));
+    return *reinterpret_cast<float2 *>(&r);
+}
+
 template <>
 __device__ __forceinline__ void unpack<DT_INT4>(const uint4 &w, float (&o)[32])
 {

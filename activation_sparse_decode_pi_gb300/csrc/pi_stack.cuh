@@ -774,6 +774,18 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             };
             // the first cold neurons' copies: copy q goes to lane q / 16 of warp q % 16 (a warp
             // issues its copies one after another, so every warp takes a few)
+            // this thread's chunks of x_l, requested before the rows (behind a full copy queue their
+            // loads would wait microseconds)
+            float4 xv[CPT][VW / 4];
+#pragma unroll
+            for (int cc = 0; cc < CPT; ++cc) {
+                const int ci = tid + cc * STACK_NT;
+#pragma unroll
+                for (int e4 = 0; e4 < VW / 4; ++e4) {
+                    xv[cc][e4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (ci < nchw) xv[cc][e4] = __ldcg(reinterpret_cast<const float4 *>(xl + (size_t)ci * VW) + e4);
+                }
+            }
             const int NPART = stage_parts<WT, KIND>(a);
             const int cq = lane * SNW + warp, cw = cq / NPART, cj = cq - cw * NPART;   // this thread's copy
             if (nh + cw < nn && cw < SC) {
@@ -781,27 +793,44 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 uint32_t par;
                 stage_part<WT, KIND>(a, Lw, ring, mbar, slot_of(nh + cw, par), sneur[nh + cw], cj);
             }
-            // this thread's columns of u, scaled (loaded while the first rows are in flight)
-            float ur[CPT][VW];
+            // this thread's columns of u, scaled; int4: as fp32 pairs (8q + i, 8q + i + 4), the
+            // pairing of the decoded nibbles (i4_word_f32x2)
+            constexpr bool I4 = WT == DT_INT4;
+            float ur[I4 ? 1 : CPT][I4 ? 1 : VW];
+            float2 ux[I4 ? CPT : 1][16];
 #pragma unroll
             for (int cc = 0; cc < CPT; ++cc) {
-                const int ci = tid + cc * STACK_NT;
+                if constexpr (I4) {
 #pragma unroll
-                for (int e4 = 0; e4 < VW / 4; ++e4) {
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (ci < nchw) v = __ldcg(reinterpret_cast<const float4 *>(xl + (size_t)ci * VW) + e4);
-                    ur[cc][4 * e4 + 0] = v.x * inv;
-                    ur[cc][4 * e4 + 1] = v.y * inv;
-                    ur[cc][4 * e4 + 2] = v.z * inv;
-                    ur[cc][4 * e4 + 3] = v.w * inv;
+                    for (int q = 0; q < 4; ++q) {
+                        ux[cc][4 * q + 0] = make_float2(xv[cc][2 * q].x * inv, xv[cc][2 * q + 1].x * inv);
+                        ux[cc][4 * q + 1] = make_float2(xv[cc][2 * q].y * inv, xv[cc][2 * q + 1].y * inv);
+                        ux[cc][4 * q + 2] = make_float2(xv[cc][2 * q].z * inv, xv[cc][2 * q + 1].z * inv);
+                        ux[cc][4 * q + 3] = make_float2(xv[cc][2 * q].w * inv, xv[cc][2 * q + 1].w * inv);
+                    }
+                } else {
+#pragma unroll
+                    for (int e4 = 0; e4 < VW / 4; ++e4) {
+                        ur[cc][4 * e4 + 0] = xv[cc][e4].x * inv;
+                        ur[cc][4 * e4 + 1] = xv[cc][e4].y * inv;
+                        ur[cc][4 * e4 + 2] = xv[cc][e4].z * inv;
+                        ur[cc][4 * e4 + 3] = xv[cc][e4].w * inv;
+                    }
                 }
             }
 
-            float yr[CPT][VW];
+            float yr[I4 ? 1 : CPT][I4 ? 1 : VW];
+            float2 yx[I4 ? CPT : 1][16];   // int4: W_down sums as pairs (8q + i, 8q + i + 4)
 #pragma unroll
-            for (int cc = 0; cc < CPT; ++cc)
+            for (int cc = 0; cc < CPT; ++cc) {
+                if constexpr (I4) {
 #pragma unroll
-                for (int e = 0; e < VW; ++e) yr[cc][e] = 0.f;
+                    for (int j = 0; j < 16; ++j) yx[cc][j] = make_float2(0.f, 0.f);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VW; ++e) yr[cc][e] = 0.f;
+                }
+            }
 
             // Neurons are reduced a batch at a time, in list order (hot ones first): one CTA-wide
             // synchronisation per batch. Hot batches take up to NB resident neurons; a cold batch
@@ -853,40 +882,28 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     for (int cc = 0; cc < CPT; ++cc) {
                         const int ci = tid + cc * STACK_NT;
                         if (ci >= nchw) break;
-                        if constexpr (WT == DT_INT4) {
-                            uint32_t ag[NB][4];
-                            float tg[NB];
+                        if constexpr (I4) {
+                            // the nibbles decoded by fp16 bit tricks (no integer-to-float conversions,
+                            // which share the integer pipe with the shifts), two FMAs per instruction:
+                            // neuron k's chain pairs columns (8q + i, 8q + i + 4), added at the end
 #pragma unroll
-                            for (int k = 0; k < NB; ++k) {
-                                const uint4 w = reinterpret_cast<const uint4 *>(sls[k])[ci];
-                                ag[k][0] = w.x; ag[k][1] = w.y; ag[k][2] = w.z; ag[k][3] = w.w;
-                                tg[k] = 0.f;
-                            }
+                            for (int g = 0; g < GI; ++g) {   // gate rows, then up rows
+                                float2 t2[NB];
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
+                                for (int k = 0; k < NB; ++k) t2[k] = make_float2(0.f, 0.f);
 #pragma unroll
-                                for (int k = 0; k < NB; ++k) tg[k] = fmaf(nib(ag[k][e >> 3], e & 7), ur[cc][e], tg[k]);
+                                for (int q = 0; q < 4; ++q)
 #pragma unroll
-                            for (int k = 0; k < NB; ++k) {
-                                const __half *ss = reinterpret_cast<const __half *>(sls[k] + ROWS * rowb);
-                                v[GI * k] = fmaf(__half2float(ss[ci >> 2]), tg[k], v[GI * k]);
-                            }
-                            if constexpr (KIND == KIND_GATED) {
+                                    for (int k = 0; k < NB; ++k) {
+                                        float2 pv[4];
+                                        i4_word_f32x2(reinterpret_cast<const uint32_t *>(sls[k] + g * rowb)[4 * ci + q], pv);
 #pragma unroll
-                                for (int k = 0; k < NB; ++k) {
-                                    const uint4 w = reinterpret_cast<const uint4 *>(sls[k] + rowb)[ci];
-                                    ag[k][0] = w.x; ag[k][1] = w.y; ag[k][2] = w.z; ag[k][3] = w.w;
-                                    tg[k] = 0.f;
-                                }
-#pragma unroll
-                                for (int e = 0; e < 32; ++e)
-#pragma unroll
-                                    for (int k = 0; k < NB; ++k)
-                                        tg[k] = fmaf(nib(ag[k][e >> 3], e & 7), ur[cc][e], tg[k]);
+                                        for (int i = 0; i < 4; ++i) t2[k] = ffma2(pv[i], ux[cc][4 * q + i], t2[k]);
+                                    }
 #pragma unroll
                                 for (int k = 0; k < NB; ++k) {
                                     const __half *ss = reinterpret_cast<const __half *>(sls[k] + ROWS * rowb);
-                                    v[GI * k + 1] = fmaf(__half2float(ss[d / 128 + (ci >> 2)]), tg[k], v[GI * k + 1]);
+                                    v[GI * k + g] = fmaf(__half2float(ss[g * (d / 128) + (ci >> 2)]), t2[k].x + t2[k].y, v[GI * k + g]);
                                 }
                             }
                         } else {
@@ -952,12 +969,18 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                         const int ci = tid + cc * STACK_NT;
                         if (ci >= nchw) break;
                         const uint4 w4 = wd[ci];
-                        if constexpr (WT == DT_INT4) {
+                        if constexpr (I4) {
                             const __half *ss = reinterpret_cast<const __half *>(sl + ROWS * rowb + (ROWS - 1) * sclb);
                             const float hs = hv * __half2float(ss[ci >> 2]);
+                            const float2 hs2 = make_float2(hs, hs);
                             const uint32_t aw[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) yr[cc][e] = fmaf(hs, nib(aw[e >> 3], e & 7), yr[cc][e]);
+                            for (int q = 0; q < 4; ++q) {
+                                float2 pv[4];
+                                i4_word_f32x2(aw[q], pv);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) yx[cc][4 * q + i] = ffma2(hs2, pv[i], yx[cc][4 * q + i]);
+                            }
                         } else {
                             float wf[VW];
                             unpack<WT>(w4, wf);
@@ -982,9 +1005,17 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 const int ci = tid + cc * STACK_NT;
                 if (ci >= nchw) break;
 #pragma unroll
-                for (int e4 = 0; e4 < VW / 4; ++e4)
-                    reinterpret_cast<float4 *>(pq + (size_t)ci * VW)[e4] =
-                        make_float4(yr[cc][4 * e4], yr[cc][4 * e4 + 1], yr[cc][4 * e4 + 2], yr[cc][4 * e4 + 3]);
+                for (int e4 = 0; e4 < VW / 4; ++e4) {
+                    float4 y4;
+                    if constexpr (I4) {   // float4 e4 holds elements 4 e4 .. 4 e4 + 3: pair halves of word e4 / 2
+                        const int q = e4 >> 1;
+                        y4 = (e4 & 1) ? make_float4(yx[cc][4 * q].y, yx[cc][4 * q + 1].y, yx[cc][4 * q + 2].y, yx[cc][4 * q + 3].y)
+                                      : make_float4(yx[cc][4 * q].x, yx[cc][4 * q + 1].x, yx[cc][4 * q + 2].x, yx[cc][4 * q + 3].x);
+                    } else {
+                        y4 = make_float4(yr[cc][4 * e4], yr[cc][4 * e4 + 1], yr[cc][4 * e4 + 2], yr[cc][4 * e4 + 3]);
+                    }
+                    reinterpret_cast<float4 *>(pq + (size_t)ci * VW)[e4] = y4;
+                }
             }
             stamp(l, 5);
         }
