@@ -190,6 +190,7 @@ struct pi_ffn {
     int stack_balance = 0;             // persistent step: FFN neurons spread evenly over the CTAs (PI_FFN_STACK_BALANCE)
     int32_t *stack_glist = nullptr, *stack_gcount = nullptr;
     int stack_pf = 1;                  // L2 prefetch of the persistent step: bit 0 P1, bit 1 unstaged P2 rows (PI_FFN_STACK_PF)
+    int stack_pf_frac = 256;           // share (of 256) of the unstaged P2 rows prefetched during the FFN (PI_FFN_STACK_PF_P2_FRAC)
     int off_ring = 0, off_flags = 0, off_mbar = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
     // tensor-core path (batch >= tc_min_b, set by plan_tc)
     bool tc_ok = false;
@@ -666,7 +667,8 @@ void plan_stack(pi_ffn_t *h)
     // after the FFN, landing during the reduction just before the predictor reads them.
     const size_t pred_bytes = elt_row_bytes(D.pdtype, D.d) * D.r + p2row * D.f;
     h->stack_pf = pred_bytes <= (40u << 20) ? 7 : 1;
-    if (const char *pf = std::getenv("PI_FFN_STACK_PF")) h->stack_pf = std::max(0, std::min(7, std::atoi(pf)));
+    if (const char *pf = std::getenv("PI_FFN_STACK_PF")) h->stack_pf = std::max(0, std::min(15, std::atoi(pf)));
+    if (const char *pr = std::getenv("PI_FFN_STACK_PF_P2_FRAC")) h->stack_pf_frac = std::max(0, std::min(256, std::atoi(pr)));
     if (const char *bl = std::getenv("PI_FFN_STACK_BALANCE")) h->stack_balance = bl[0] == '0' ? 0 : 1;
     if (const char *ps = std::getenv("PI_FFN_STACK_P2_STAGE")) h->stack_p2_stage = std::max(0, std::atoi(ps));
     h->stack_ok = true;
@@ -714,6 +716,8 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.p2_stage_tiles = h->stack_p2_stage;
     a.pf_p1 = (h->stack_pf & 4) ? 2 : (h->stack_pf & 1);   // 2: a layer ahead, 1: just in time
     a.pf_p2 = (h->stack_pf >> 1) & 1;
+    a.pf_p2_ffn = (h->stack_pf >> 3) & 1;
+    a.pf_p2_frac = h->stack_pf_frac;
     a.balance = h->stack_balance && a.hot_k == 0 ? 1 : 0;
     a.glist = h->stack_glist;
     a.gcount = h->stack_gcount;

@@ -125,6 +125,12 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// One 128-byte line into L2 (a hint: no completion, no fault on a valid address).
+__device__ __forceinline__ void prefetch_line_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void prefetch_l2_range(const void *src, size_t bytes)
 {
     const char *p = (const char *)src;

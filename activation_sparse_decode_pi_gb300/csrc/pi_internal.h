@@ -89,6 +89,8 @@ struct StackArgs {
     int p2_stage_tiles;           // of which filled between layers, at most (the rest as the logits start)
     int pf_p1;                    // the next layer's P1 rows into L2: 1 during the grid barrier after the FFN, 2 a layer ahead
     int pf_p2;                    // the next layer's unstaged P2 rows into L2 a layer ahead
+    int pf_p2_ffn;                // the next layer's unstaged P2 rows into L2 during this layer's FFN, the first pf_p2_frac / 256 of them
+    int pf_p2_frac;
     int balance;                  // spread the FFN's neurons evenly over the CTAs (one more grid barrier per layer)
     int32_t *glist, *gcount;      // [grid x STACK_MAX_CHUNK] published lists, [grid] their counts
     float *x_layers;              // optional [L x d]: row l = x_{l+1} (every layer's output), or NULL

@@ -635,8 +635,12 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                                 s_p2iss[j] += 1;
                                 mbar_arrive_expect_tx(&s_p2bar[j], tile_bytes(tn));
                             }
-                            if (gtid >= 64 && gtid < 80)
-                                copy_tile_rows(Lw.p2, tn, j, tn * 16 + gtid - 64, tn * 16 + gtid - 63);
+                            // two lanes of each of the group's 8 warps: a warp's bulk copies run one after
+                            // another, so the 16 copies of a tile are spread over the warps
+                            if (lane == 20 || lane == 21) {
+                                const int q = gw * 2 + lane - 20;
+                                copy_tile_rows(Lw.p2, tn, j, tn * 16 + q, tn * 16 + q + 1);
+                            }
                         }
                         j += 2;
                         if (j >= RT) {
@@ -792,6 +796,15 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 fence_proxy_async_smem();
                 uint32_t par;
                 stage_part<WT, KIND>(a, Lw, ring, mbar, slot_of(nh + cw, par), sneur[nh + cw], cj);
+            }
+            // The next layer's P2 rows that its logits will stream (not staged in the ring) into L2
+            // while the FFN leaves the DRAM mostly idle (128-byte lines spread over the threads).
+            if (a.pf_p2_ffn && l + 1 < a.L) {
+                const int lines = (r * pb + 127) >> 7, kh = KS + (int)(((long long)(K - KS) * a.pf_p2_frac) >> 8);
+                for (int j = tid; j < (kh - KS) * lines; j += STACK_NT) {
+                    const int k = KS + j / lines;
+                    prefetch_line_l2((const char *)s_p2next + (size_t)(c + (size_t)P * k) * r * pb + 128 * (j % lines));
+                }
             }
             // this thread's columns of u, scaled; int4: as fp32 pairs (8q + i, 8q + i + 4), the
             // pairing of the decoded nibbles (i4_word_f32x2)
