@@ -189,6 +189,7 @@ struct pi_ffn {
     int stack_p2_stage = STACK_P2_TILES;   // P2 tiles filled between layers, at most (PI_FFN_STACK_P2_STAGE)
     int stack_balance = 0;             // persistent step: FFN neurons spread evenly over the CTAs (PI_FFN_STACK_BALANCE)
     int32_t *stack_glist = nullptr, *stack_gcount = nullptr;
+    unsigned long long *stack_gflag = nullptr;
     int stack_pf = 1;                  // L2 prefetch of the persistent step: bit 0 P1, bit 1 unstaged P2 rows (PI_FFN_STACK_PF)
     int stack_pf_frac = 256;           // share (of 256) of the unstaged P2 rows prefetched during the FFN (PI_FFN_STACK_PF_P2_FRAC)
     int off_ring = 0, off_flags = 0, off_mbar = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
@@ -669,7 +670,10 @@ void plan_stack(pi_ffn_t *h)
     h->stack_pf = pred_bytes <= (40u << 20) ? 7 : 1;
     if (const char *pf = std::getenv("PI_FFN_STACK_PF")) h->stack_pf = std::max(0, std::min(15, std::atoi(pf)));
     if (const char *pr = std::getenv("PI_FFN_STACK_PF_P2_FRAC")) h->stack_pf_frac = std::max(0, std::min(256, std::atoi(pr)));
-    if (const char *bl = std::getenv("PI_FFN_STACK_BALANCE")) h->stack_balance = bl[0] == '0' ? 0 : 1;
+    if (const char *bl = std::getenv("PI_FFN_STACK_BALANCE")) {
+        const int v = std::atoi(bl);
+        h->stack_balance = v == 2 || v == 4 || v == 8 ? v : (v ? 1 : 0);
+    }
     if (const char *ps = std::getenv("PI_FFN_STACK_P2_STAGE")) h->stack_p2_stage = std::max(0, std::atoi(ps));
     h->stack_ok = true;
 }
@@ -718,9 +722,11 @@ cudaError_t launch_stack(const pi_ffn_t *h, const float *x0, float *x_out, int32
     a.pf_p2 = (h->stack_pf >> 1) & 1;
     a.pf_p2_ffn = (h->stack_pf >> 3) & 1;
     a.pf_p2_frac = h->stack_pf_frac;
-    a.balance = h->stack_balance && a.hot_k == 0 ? 1 : 0;
+    a.balance = a.hot_k == 0 && (h->stack_balance == 1 || (h->stack_balance > 1 && h->nsm % h->stack_balance == 0))
+                    ? h->stack_balance : 0;
     a.glist = h->stack_glist;
     a.gcount = h->stack_gcount;
+    a.gflag = h->stack_gflag;
     a.x_layers = x_layers;
     a.stamps = h->phase_stamps;
     a.bias_bulk = D.f % 4 == 0 ? 1 : 0;
@@ -807,6 +813,7 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
         h->tc_ok ? (size_t)(h->tc_ntiles + 1) * 4 : 0, // tc_cnt
         (size_t)h->nsm * STACK_MAX_CHUNK * 4,          // stack_glist
         (size_t)h->nsm * 4,                            // stack_gcount
+        (size_t)h->nsm * 8,                            // stack_gflag
     };
     const int nbuf = sizeof(sizes) / sizeof(sizes[0]);
     size_t off[32], total = 0;
@@ -853,6 +860,7 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
     }
     h->stack_glist = (int32_t *)(base + off[24]);
     h->stack_gcount = (int32_t *)(base + off[25]);
+    h->stack_gflag = (unsigned long long *)(base + off[26]);
     {
         std::vector<StackLayer> sl(D.n_layers);
         for (int l = 0; l < D.n_layers; ++l) {
@@ -1071,6 +1079,9 @@ pi_status_t pi_get_status(pi_ffn_t *h)
     if (v && cudaMemset(h->status, 0, 4) != cudaSuccess) return cuda_status(cudaGetLastError());
     // a grid barrier that gave up leaves its arrival count behind: start the next step clean
     if (v == PI_ERR_TIMEOUT && cudaMemset(h->tickets + 2, 0, 8) != cudaSuccess) return cuda_status(cudaGetLastError());
+    // the group exchange's epochs derive from the barrier counter: restart them with it
+    if (v == PI_ERR_TIMEOUT && h->stack_gflag && cudaMemset(h->stack_gflag, 0, (size_t)h->nsm * 8) != cudaSuccess)
+        return cuda_status(cudaGetLastError());
     // so does a tensor-core kernel that gave up between its tile tickets
     if (v == PI_ERR_TIMEOUT && h->tc_cnt &&
         cudaMemset(h->tc_cnt, 0, (size_t)(h->tc_ntiles + 1) * 4) != cudaSuccess)

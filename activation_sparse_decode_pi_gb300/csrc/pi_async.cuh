@@ -152,6 +152,24 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
     return v;
 }
 
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Wait (bounded) until *p >= v (a value another CTA of the same launch publishes with a release
+// store); false after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool wait_flag_ge(const unsigned long long *p, unsigned long long v)
+{
+    if ((long long)(ld_acquire_u64(p) - v) >= 0) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while ((long long)(ld_acquire_u64(p) - v) < 0) {
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+        __nanosleep(32);
+    }
+    return true;
+}
+
 __device__ __forceinline__ void red_release_add_u64(unsigned long long *p, unsigned long long v)
 {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");

@@ -91,8 +91,9 @@ struct StackArgs {
     int pf_p2;                    // the next layer's unstaged P2 rows into L2 a layer ahead
     int pf_p2_ffn;                // the next layer's unstaged P2 rows into L2 during this layer's FFN, the first pf_p2_frac / 256 of them
     int pf_p2_frac;
-    int balance;                  // spread the FFN's neurons evenly over the CTAs (one more grid barrier per layer)
+    int balance;                  // spread the FFN's neurons evenly: 1 over all CTAs (one more grid barrier per layer), 2/4/8 within groups of as many CTAs
     int32_t *glist, *gcount;      // [grid x STACK_MAX_CHUNK] published lists, [grid] their counts
+    unsigned long long *gflag;    // [grid] per CTA: the last (launch, layer) epoch whose list it published
     float *x_layers;              // optional [L x d]: row l = x_{l+1} (every layer's output), or NULL
     unsigned long long *stamps;   // optional [L x STACK_PHASES x grid] %globaltimer stamps, or NULL
 };

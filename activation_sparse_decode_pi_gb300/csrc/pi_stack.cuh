@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
         for (int j = 0; j < RT && j < STACK_P2_TILES; ++j) mbar_init(&s_p2bar[j], 1);
         fence_mbar_init();
         s_pend = a.hot_k > 0 ? 0 : -1;
-        s_base = barrier_base(a.bar, (unsigned long long)((3 + (a.balance ? 1 : 0)) * a.L) * a.nblocks);
+        s_base = barrier_base(a.bar, (unsigned long long)((3 + (a.balance == 1 ? 1 : 0)) * a.L) * a.nblocks);
     }
     if (tid < STACK_P2_TILES) {
         s_p2use[tid] = tid < min(MTS, RT) ? (MTS - tid + RT - 1) / RT : 0;
@@ -716,7 +716,52 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             }
             if (tid == 0 && a.counts && nn) atomicAdd(a.counts + l, nn);
             __syncthreads();
-            if (a.balance) {
+            if (a.balance > 1) {
+                // Within each group of G consecutive CTAs: every member publishes its list and an
+                // epoch (this launch and layer), waits for the other members' epochs, and takes an
+                // equal share (positions [r N / G, (r + 1) N / G) for member r) of the group's lists
+                // concatenated in member order. No grid barrier; the slowest member of a group has
+                // the mean of G counts instead of its own. Deterministic: fixed by the lists alone.
+                const int G = a.balance, g0 = c & ~(G - 1), rk = c - g0;
+                const unsigned long long epoch = s_base + (unsigned long long)(l + 1);
+                int32_t *gl = a.glist + (size_t)c * STACK_MAX_CHUNK;
+                for (int m = tid; m < nn; m += STACK_NT) gl[m] = sneur[m];
+                if (tid == 0) a.gcount[c] = nn;
+                __syncthreads();   // the CTA's list stores come before the release below
+                if (tid == 0) {
+                    __threadfence();
+                    st_release_u64(a.gflag + c, epoch);
+                }
+                bool okw = true;
+                if (tid < G && tid != rk) okw = wait_flag_ge(a.gflag + g0 + tid, epoch);
+                if (!__syncthreads_and(okw)) {
+                    if (tid == 0) set_status(a.status, ST_TIMEOUT);
+                    return;
+                }
+                int *pref = reinterpret_cast<int *>(spb);   // [G + 1]; the logits' biases are dead now
+                if (tid == 0) {
+                    int run = 0;
+                    for (int q = 0; q < G; ++q) {
+                        pref[q] = run;
+                        run += __ldcg(a.gcount + g0 + q);
+                    }
+                    pref[G] = run;
+                }
+                __syncthreads();
+                const int N = pref[G];
+                const int lo = (int)((long long)rk * N / G);
+                nn = (int)((long long)(rk + 1) * N / G) - lo;
+                for (int m = tid; m < nn; m += STACK_NT) {
+                    const int q = lo + m;
+                    int a0 = 0;   // pref[a0] <= q < pref[a0 + 1]
+                    while (a0 + 1 < G && pref[a0 + 1] <= q) ++a0;
+                    const int i = __ldcg(a.glist + (size_t)(g0 + a0) * STACK_MAX_CHUNK + (q - pref[a0]));
+                    sneur[m] = i;
+                    if (!bias_bulk) sbias[m] = Lw.bg ? __ldg(Lw.bg + i) : 0.f;
+                }
+                __syncthreads();
+            }
+            if (a.balance == 1) {
                 // Every CTA publishes its list; after one more grid barrier each takes an equal share
                 // (positions [c N / P, (c + 1) N / P)) of the lists concatenated in CTA order, so the
                 // FFN's rows are spread evenly over the SMs whatever the per-CTA counts. The order

@@ -35,14 +35,17 @@
  *                           persistent one-kernel step.
  *  - PI_FFN_STACK_P2=0      the persistent step reads the predictor's P2 rows from memory
  *                           instead of passing them through its shared-memory ring.
- *  - PI_FFN_STACK_BALANCE=0 the persistent step computes each CTA's own active neurons instead
- *                           of spreading the layer's active neurons evenly over the CTAs
- *                           (which costs one more grid barrier per layer).
+ *  - PI_FFN_STACK_BALANCE=n the persistent step spreads the layer's active neurons evenly: 1
+ *                           over all CTAs (one more grid barrier per layer), 2, 4 or 8 within
+ *                           groups of as many consecutive CTAs (the members exchange their lists
+ *                           through memory, no grid barrier); 0 (the default): each CTA computes
+ *                           its own active neurons.
  *  - PI_FFN_STACK_PF=n      L2 prefetches of the persistent step, a bit mask: 1 = the next
  *                           layer's P1 rows (during the grid barrier after the FFN, or a whole
  *                           layer ahead with 4), 2 = the next layer's P2 rows that the ring does
- *                           not hold, a whole layer ahead. Default 7 while one layer's predictor
- *                           is at most 40 MB, else 1.
+ *                           not hold, a whole layer ahead, 8 = those rows during this layer's
+ *                           FFN (the first PI_FFN_STACK_PF_P2_FRAC / 256 of them, default all).
+ *                           Default 7 while one layer's predictor is at most 40 MB, else 1.
  *  - PI_FFN_STACK_P2_STAGE=n  at most n P2 tiles are copied into the ring between layers (the
  *                           rest as the logits start); default all that fit.
  *  - PI_FFN_TC=0            every batch > 1 stays on the CUDA-core kernels.
