@@ -324,6 +324,25 @@ def test_decode_stack_both_paths_batch1(P, wi, shape):
         ffn.close()
 
 
+@pytest.mark.parametrize("group", ["1", "2", "8"])
+@pytest.mark.parametrize("wi", [1, 3, 4])
+def test_decode_stack_spread_neurons(P, wi, group):
+    """The FFN's active neurons spread over all CTAs (one more grid barrier) or within groups of 2
+    and 8 CTAs (lists exchanged through memory): the same layers against the oracle, teacher-forced,
+    and repeated steps give the same bits."""
+    w = _wl(wi, STACK_SHAPE, n_layers=3)
+    layers = build_layers(w, range(w.n_layers))
+    X = make_inputs(w, 2, 1, seed=31, device="cpu").numpy()
+    ffn = _with_env("PI_FFN_STACK_BALANCE", group, lambda: _handle(P, w, [g for g, _ in layers], stack_kernel=True))
+    P.pi_profile_begin(ffn.h)
+    ffn.decode_stack(to_dev(X[0]))
+    prof = P.pi_profile_end(ffn.h)
+    assert prof["decode_stack"][1] == 1, prof
+    _stack_vs_oracle(P, w, layers, X, ffn, (wi, group))
+    assert ffn.status() == 0
+    ffn.close()
+
+
 @pytest.mark.parametrize("wi", [1, 3, 4])
 def test_decode_stack_tc_logits_many_tiles(P, wi):
     """~300 owned P2 rows per CTA, all staged: more 16-row tiles than warps, each warp taking
@@ -460,6 +479,25 @@ def test_decode_stack_p2_staging_bit_identical(P, wi, shape):
         # and the staged kernel against the oracle, layer by layer
         _stack_vs_oracle(P, w, layers, X, staged, ("staged", wi, H), hot_prefix=H)
     for ffn in (staged, plain):
+        assert ffn.status() == 0
+        ffn.close()
+
+
+@pytest.mark.parametrize("pf", ["0", "3", "9"])
+def test_decode_stack_prefetch_bits(P, pf):
+    """The L2 prefetches (P1 and P2 a layer ahead, the streamed P2 rows during the FFN, none) are
+    hints: the output bits are those of the default setting."""
+    w = _wl(3, P2_WIDE_SHAPE, n_layers=3)
+    layers = build_layers(w, range(w.n_layers))
+    X = make_inputs(w, 2, 1, seed=17, device="cpu").numpy()
+    ref = _handle(P, w, [g for g, _ in layers], stack_kernel=True)
+    alt = _with_env("PI_FFN_STACK_PF", pf, lambda: _handle(P, w, [g for g, _ in layers], stack_kernel=True))
+    for t in range(X.shape[0]):
+        a = ref.decode_stack(to_dev(X[t])).clone()
+        b = alt.decode_stack(to_dev(X[t])).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(a, b), (pf, t)
+    for ffn in (ref, alt):
         assert ffn.status() == 0
         ffn.close()
 
