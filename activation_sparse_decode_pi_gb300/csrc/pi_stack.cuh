@@ -1006,44 +1006,96 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     if (sk < 0) sk += SC;
                     stage_part<WT, KIND>(a, Lw, ring, mbar, HK + sk, sneur[m0 - nbc + cw + SC], cj);
                 }
+                // The batch's sums, all its neurons at once (one shuffle chain instead of one per
+                // neuron): lane (w, h) = (lane & 15, lane >> 4) holds warp w's partials of values h,
+                // h + 2, ... (value v = GI k + g: gated g = 0 gate, g = 1 up; else v = k), each added
+                // over the 16 warps in a fixed butterfly order, so that value v ends in lane
+                // 16 (v & 1), register v / 2, with the same bits as one neuron at a time.
+                constexpr int GV = KIND == KIND_GATED ? 2 : 1, NH = NV / 2;
+                float sv[NH];
+#pragma unroll
+                for (int j = 0; j < NH; ++j) sv[j] = red[bi & 1][lane & 15][2 * j + (lane >> 4)];
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1)
+#pragma unroll
+                    for (int j = 0; j < NH; ++j) sv[j] += __shfl_xor_sync(0xffffffffu, sv[j], o);
+                float hvb[NB];   // h of the batch's neurons (0 past the batch's end)
 #pragma unroll
                 for (int k = 0; k < NB; ++k) {
-                    if (k >= mb) break;
-                    uint32_t par;
-                    const unsigned char *sl = ring + (size_t)slot_at(m0, cold, k, par) * a.slot_bytes;
-                    // neuron k's partial sums of the 16 warps, added in a fixed butterfly order
-                    float sg = KIND == KIND_GATED ? red[bi & 1][lane & 15][2 * k + (lane >> 4)] : red[bi & 1][lane & 15][k];
-                    sg += __shfl_xor_sync(0xffffffffu, sg, 8);
-                    sg += __shfl_xor_sync(0xffffffffu, sg, 4);
-                    sg += __shfl_xor_sync(0xffffffffu, sg, 2);
-                    sg += __shfl_xor_sync(0xffffffffu, sg, 1);
-                    float g = __shfl_sync(0xffffffffu, sg, 0);
-                    g += bias_bulk ? reinterpret_cast<const float *>(sl + bias_off)[sneur[m0 + k] & 3] : sbias[m0 + k];
+                    const int v = GV * k, mk = k < mb ? m0 + k : m0;
+                    float g = __shfl_sync(0xffffffffu, sv[v >> 1], 16 * (v & 1));
+                    g += bias_bulk ? reinterpret_cast<const float *>(sls[k] + bias_off)[sneur[mk] & 3] : sbias[mk];
                     float hv = fmaxf(g, 0.f);
-                    if (KIND == KIND_GATED) hv *= __shfl_sync(0xffffffffu, sg, 16);
-                    const uint4 *wd = reinterpret_cast<const uint4 *>(sl + (ROWS - 1) * rowb);
+                    if (KIND == KIND_GATED) hv *= __shfl_sync(0xffffffffu, sv[(v + 1) >> 1], 16 * ((v + 1) & 1));
+                    hvb[k] = k < mb ? hv : 0.f;
+                }
+                // W_down: every output element takes the batch's neurons in list order (the same
+                // bits as one neuron at a time); a full batch interleaves the neurons' rows.
+                if (mb == NB) {
 #pragma unroll
                     for (int cc = 0; cc < CPT; ++cc) {
                         const int ci = tid + cc * STACK_NT;
                         if (ci >= nchw) break;
-                        const uint4 w4 = wd[ci];
+                        uint4 w4[NB];
+#pragma unroll
+                        for (int k = 0; k < NB; ++k) w4[k] = reinterpret_cast<const uint4 *>(sls[k] + (ROWS - 1) * rowb)[ci];
                         if constexpr (I4) {
-                            const __half *ss = reinterpret_cast<const __half *>(sl + ROWS * rowb + (ROWS - 1) * sclb);
-                            const float hs = hv * __half2float(ss[ci >> 2]);
-                            const float2 hs2 = make_float2(hs, hs);
-                            const uint32_t aw[4] = {w4.x, w4.y, w4.z, w4.w};
+                            float hs[NB];
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                float2 pv[4];
-                                i4_word_f32x2(aw[q], pv);
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) yx[cc][4 * q + i] = ffma2(hs2, pv[i], yx[cc][4 * q + i]);
+                            for (int k = 0; k < NB; ++k) {
+                                const __half *ss = reinterpret_cast<const __half *>(sls[k] + ROWS * rowb + (ROWS - 1) * sclb);
+                                hs[k] = hvb[k] * __half2float(ss[ci >> 2]);
                             }
-                        } else {
-                            float wf[VW];
-                            unpack<WT>(w4, wf);
 #pragma unroll
-                            for (int e = 0; e < VW; ++e) yr[cc][e] = fmaf(hv, wf[e], yr[cc][e]);
+                            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                                for (int k = 0; k < NB; ++k) {
+                                    const uint32_t wq = q == 0 ? w4[k].x : q == 1 ? w4[k].y : q == 2 ? w4[k].z : w4[k].w;
+                                    const float2 hs2 = make_float2(hs[k], hs[k]);
+                                    float2 pv[4];
+                                    i4_word_f32x2(wq, pv);
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) yx[cc][4 * q + i] = ffma2(hs2, pv[i], yx[cc][4 * q + i]);
+                                }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < NB; ++k) {
+                                float wf[VW];
+                                unpack<WT>(w4[k], wf);
+#pragma unroll
+                                for (int e = 0; e < VW; ++e) yr[cc][e] = fmaf(hvb[k], wf[e], yr[cc][e]);
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < NB; ++k) {
+                        if (k >= mb) break;
+                        const unsigned char *sl = sls[k];
+                        const uint4 *wd = reinterpret_cast<const uint4 *>(sl + (ROWS - 1) * rowb);
+#pragma unroll
+                        for (int cc = 0; cc < CPT; ++cc) {
+                            const int ci = tid + cc * STACK_NT;
+                            if (ci >= nchw) break;
+                            const uint4 w4 = wd[ci];
+                            if constexpr (I4) {
+                                const __half *ss = reinterpret_cast<const __half *>(sl + ROWS * rowb + (ROWS - 1) * sclb);
+                                const float hs = hvb[k] * __half2float(ss[ci >> 2]);
+                                const float2 hs2 = make_float2(hs, hs);
+                                const uint32_t aw[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    float2 pv[4];
+                                    i4_word_f32x2(aw[q], pv);
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) yx[cc][4 * q + i] = ffma2(hs2, pv[i], yx[cc][4 * q + i]);
+                                }
+                            } else {
+                                float wf[VW];
+                                unpack<WT>(w4, wf);
+#pragma unroll
+                                for (int e = 0; e < VW; ++e) yr[cc][e] = fmaf(hvb[k], wf[e], yr[cc][e]);
+                            }
                         }
                     }
                 }
