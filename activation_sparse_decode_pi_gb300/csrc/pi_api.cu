@@ -610,8 +610,8 @@ void plan_stack(pi_ffn_t *h)
                        (D.wdtype == PI_F16 && D.pdtype == PI_F16) ||
                        (D.wdtype == PI_INT4_G128 && (D.pdtype == PI_F16 || D.pdtype == PI_BF16));
     if (!combo) return;
-    const int V = D.wdtype == PI_F32 ? 4 : (D.wdtype == PI_INT4_G128 ? 32 : 8);
-    const int cpt = D.wdtype == PI_INT4_G128 ? 1 : 3;
+    const int V = D.wdtype == PI_F32 ? 4 : 8;                      // columns per unit of the FFN's thread mapping
+    const int cpt = D.wdtype == PI_INT4_G128 ? 4 : 3;                  // units per thread (kernel instances)
     if (D.d % V || D.d / V > cpt * STACK_NT) return;
     if (D.wdtype == PI_INT4_G128) {
         if (D.d % 1024) return;                                    // scale rows must be 16-byte multiples

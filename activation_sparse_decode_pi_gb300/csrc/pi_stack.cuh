@@ -232,7 +232,6 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
     const int P = gridDim.x, c = blockIdx.x;
     const int d = a.d, f = a.f, r = a.r, S = a.slots;
     const int W = (f + 31) >> 5;
-    const int nchw = d / VW;
     const int rowb = weight_row_bytes<WT>(d);
     const int sclb = WT == DT_INT4 ? (d / 128) * 2 : 0;
     const int pb = PT == DT_F32 ? 4 : 2;
@@ -823,16 +822,22 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             };
             // the first cold neurons' copies: copy q goes to lane q / 16 of warp q % 16 (a warp
             // issues its copies one after another, so every warp takes a few)
-            // this thread's chunks of x_l, requested before the rows (behind a full copy queue their
-            // loads would wait microseconds)
-            float4 xv[CPT][VW / 4];
+            // The FFN's thread mapping: unit ci = tid + cc * STACK_NT (cc < CPT) of UW columns; int4:
+            // one 32-bit word of a row (8 columns) per unit, so that all 16 warps take part and a
+            // warp's loads of a row are 128 consecutive bytes; else one 16-byte chunk.
+            // This thread's units of x_l are requested before the rows (behind a full copy queue
+            // their loads would wait microseconds).
+            constexpr bool I4 = WT == DT_INT4;
+            constexpr int UW = I4 ? 8 : VW;
+            const int nunit = d / UW;
+            float4 xv[CPT][UW / 4];
 #pragma unroll
             for (int cc = 0; cc < CPT; ++cc) {
                 const int ci = tid + cc * STACK_NT;
 #pragma unroll
-                for (int e4 = 0; e4 < VW / 4; ++e4) {
+                for (int e4 = 0; e4 < UW / 4; ++e4) {
                     xv[cc][e4] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (ci < nchw) xv[cc][e4] = __ldcg(reinterpret_cast<const float4 *>(xl + (size_t)ci * VW) + e4);
+                    if (ci < nunit) xv[cc][e4] = __ldcg(reinterpret_cast<const float4 *>(xl + (size_t)ci * UW) + e4);
                 }
             }
             const int NPART = stage_parts<WT, KIND>(a);
@@ -851,21 +856,17 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     prefetch_line_l2((const char *)s_p2next + (size_t)(c + (size_t)P * k) * r * pb + 128 * (j % lines));
                 }
             }
-            // this thread's columns of u, scaled; int4: as fp32 pairs (8q + i, 8q + i + 4), the
-            // pairing of the decoded nibbles (i4_word_f32x2)
-            constexpr bool I4 = WT == DT_INT4;
+            // this thread's columns of u, scaled; int4: as fp32 pairs (i, i + 4) of its word's 8
+            // columns, the pairing of the decoded nibbles (i4_word_f32x2)
             float ur[I4 ? 1 : CPT][I4 ? 1 : VW];
-            float2 ux[I4 ? CPT : 1][16];
+            float2 ux[I4 ? CPT : 1][4];
 #pragma unroll
             for (int cc = 0; cc < CPT; ++cc) {
                 if constexpr (I4) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        ux[cc][4 * q + 0] = make_float2(xv[cc][2 * q].x * inv, xv[cc][2 * q + 1].x * inv);
-                        ux[cc][4 * q + 1] = make_float2(xv[cc][2 * q].y * inv, xv[cc][2 * q + 1].y * inv);
-                        ux[cc][4 * q + 2] = make_float2(xv[cc][2 * q].z * inv, xv[cc][2 * q + 1].z * inv);
-                        ux[cc][4 * q + 3] = make_float2(xv[cc][2 * q].w * inv, xv[cc][2 * q + 1].w * inv);
-                    }
+                    ux[cc][0] = make_float2(xv[cc][0].x * inv, xv[cc][1].x * inv);
+                    ux[cc][1] = make_float2(xv[cc][0].y * inv, xv[cc][1].y * inv);
+                    ux[cc][2] = make_float2(xv[cc][0].z * inv, xv[cc][1].z * inv);
+                    ux[cc][3] = make_float2(xv[cc][0].w * inv, xv[cc][1].w * inv);
                 } else {
 #pragma unroll
                     for (int e4 = 0; e4 < VW / 4; ++e4) {
@@ -878,12 +879,12 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             }
 
             float yr[I4 ? 1 : CPT][I4 ? 1 : VW];
-            float2 yx[I4 ? CPT : 1][16];   // int4: W_down sums as pairs (8q + i, 8q + i + 4)
+            float2 yx[I4 ? CPT : 1][4];   // int4: W_down sums as pairs (i, i + 4) of the word's columns
 #pragma unroll
             for (int cc = 0; cc < CPT; ++cc) {
                 if constexpr (I4) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) yx[cc][j] = make_float2(0.f, 0.f);
+                    for (int j = 0; j < 4; ++j) yx[cc][j] = make_float2(0.f, 0.f);
                 } else {
 #pragma unroll
                     for (int e = 0; e < VW; ++e) yr[cc][e] = 0.f;
@@ -939,29 +940,26 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 #pragma unroll
                     for (int cc = 0; cc < CPT; ++cc) {
                         const int ci = tid + cc * STACK_NT;
-                        if (ci >= nchw) break;
+                        if (ci >= nunit) break;
                         if constexpr (I4) {
                             // the nibbles decoded by fp16 bit tricks (no integer-to-float conversions,
                             // which share the integer pipe with the shifts), two FMAs per instruction:
-                            // neuron k's chain pairs columns (8q + i, 8q + i + 4), added at the end
+                            // neuron k's chain pairs columns (i, i + 4) of the word, then one scale
+                            // (group ci / 16 of 128 columns) per word
 #pragma unroll
                             for (int g = 0; g < GI; ++g) {   // gate rows, then up rows
-                                float2 t2[NB];
+                                uint32_t wv[NB];
 #pragma unroll
-                                for (int k = 0; k < NB; ++k) t2[k] = make_float2(0.f, 0.f);
-#pragma unroll
-                                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                                    for (int k = 0; k < NB; ++k) {
-                                        float2 pv[4];
-                                        i4_word_f32x2(reinterpret_cast<const uint32_t *>(sls[k] + g * rowb)[4 * ci + q], pv);
-#pragma unroll
-                                        for (int i = 0; i < 4; ++i) t2[k] = ffma2(pv[i], ux[cc][4 * q + i], t2[k]);
-                                    }
+                                for (int k = 0; k < NB; ++k) wv[k] = reinterpret_cast<const uint32_t *>(sls[k] + g * rowb)[ci];
 #pragma unroll
                                 for (int k = 0; k < NB; ++k) {
+                                    float2 pv[4];
+                                    i4_word_f32x2(wv[k], pv);
+                                    float2 t2 = make_float2(pv[0].x * ux[cc][0].x, pv[0].y * ux[cc][0].y);
+#pragma unroll
+                                    for (int i = 1; i < 4; ++i) t2 = ffma2(pv[i], ux[cc][i], t2);
                                     const __half *ss = reinterpret_cast<const __half *>(sls[k] + ROWS * rowb);
-                                    v[GI * k + g] = fmaf(__half2float(ss[g * (d / 128) + (ci >> 2)]), t2[k].x + t2[k].y, v[GI * k + g]);
+                                    v[GI * k + g] = fmaf(__half2float(ss[g * (d / 128) + (ci >> 4)]), t2.x + t2.y, v[GI * k + g]);
                                 }
                             }
                         } else {
@@ -1035,29 +1033,28 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 #pragma unroll
                     for (int cc = 0; cc < CPT; ++cc) {
                         const int ci = tid + cc * STACK_NT;
-                        if (ci >= nchw) break;
-                        uint4 w4[NB];
-#pragma unroll
-                        for (int k = 0; k < NB; ++k) w4[k] = reinterpret_cast<const uint4 *>(sls[k] + (ROWS - 1) * rowb)[ci];
+                        if (ci >= nunit) break;
                         if constexpr (I4) {
+                            uint32_t w32[NB];
                             float hs[NB];
 #pragma unroll
                             for (int k = 0; k < NB; ++k) {
+                                w32[k] = reinterpret_cast<const uint32_t *>(sls[k] + (ROWS - 1) * rowb)[ci];
                                 const __half *ss = reinterpret_cast<const __half *>(sls[k] + ROWS * rowb + (ROWS - 1) * sclb);
-                                hs[k] = hvb[k] * __half2float(ss[ci >> 2]);
+                                hs[k] = hvb[k] * __half2float(ss[ci >> 4]);
                             }
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
+                            for (int k = 0; k < NB; ++k) {
+                                const float2 hs2 = make_float2(hs[k], hs[k]);
+                                float2 pv[4];
+                                i4_word_f32x2(w32[k], pv);
 #pragma unroll
-                                for (int k = 0; k < NB; ++k) {
-                                    const uint32_t wq = q == 0 ? w4[k].x : q == 1 ? w4[k].y : q == 2 ? w4[k].z : w4[k].w;
-                                    const float2 hs2 = make_float2(hs[k], hs[k]);
-                                    float2 pv[4];
-                                    i4_word_f32x2(wq, pv);
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i) yx[cc][4 * q + i] = ffma2(hs2, pv[i], yx[cc][4 * q + i]);
-                                }
+                                for (int i = 0; i < 4; ++i) yx[cc][i] = ffma2(hs2, pv[i], yx[cc][i]);
+                            }
                         } else {
+                            uint4 w4[NB];
+#pragma unroll
+                            for (int k = 0; k < NB; ++k) w4[k] = reinterpret_cast<const uint4 *>(sls[k] + (ROWS - 1) * rowb)[ci];
 #pragma unroll
                             for (int k = 0; k < NB; ++k) {
                                 float wf[VW];
@@ -1072,27 +1069,21 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     for (int k = 0; k < NB; ++k) {
                         if (k >= mb) break;
                         const unsigned char *sl = sls[k];
-                        const uint4 *wd = reinterpret_cast<const uint4 *>(sl + (ROWS - 1) * rowb);
 #pragma unroll
                         for (int cc = 0; cc < CPT; ++cc) {
                             const int ci = tid + cc * STACK_NT;
-                            if (ci >= nchw) break;
-                            const uint4 w4 = wd[ci];
+                            if (ci >= nunit) break;
                             if constexpr (I4) {
                                 const __half *ss = reinterpret_cast<const __half *>(sl + ROWS * rowb + (ROWS - 1) * sclb);
-                                const float hs = hvb[k] * __half2float(ss[ci >> 2]);
+                                const float hs = hvb[k] * __half2float(ss[ci >> 4]);
                                 const float2 hs2 = make_float2(hs, hs);
-                                const uint32_t aw[4] = {w4.x, w4.y, w4.z, w4.w};
+                                float2 pv[4];
+                                i4_word_f32x2(reinterpret_cast<const uint32_t *>(sl + (ROWS - 1) * rowb)[ci], pv);
 #pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    float2 pv[4];
-                                    i4_word_f32x2(aw[q], pv);
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i) yx[cc][4 * q + i] = ffma2(hs2, pv[i], yx[cc][4 * q + i]);
-                                }
+                                for (int i = 0; i < 4; ++i) yx[cc][i] = ffma2(hs2, pv[i], yx[cc][i]);
                             } else {
                                 float wf[VW];
-                                unpack<WT>(w4, wf);
+                                unpack<WT>(reinterpret_cast<const uint4 *>(sl + (ROWS - 1) * rowb)[ci], wf);
 #pragma unroll
                                 for (int e = 0; e < VW; ++e) yr[cc][e] = fmaf(hvb[k], wf[e], yr[cc][e]);
                             }
@@ -1113,18 +1104,17 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
 #pragma unroll
             for (int cc = 0; cc < CPT; ++cc) {
                 const int ci = tid + cc * STACK_NT;
-                if (ci >= nchw) break;
+                if (ci >= nunit) break;
 #pragma unroll
-                for (int e4 = 0; e4 < VW / 4; ++e4) {
+                for (int e4 = 0; e4 < UW / 4; ++e4) {
                     float4 y4;
-                    if constexpr (I4) {   // float4 e4 holds elements 4 e4 .. 4 e4 + 3: pair halves of word e4 / 2
-                        const int q = e4 >> 1;
-                        y4 = (e4 & 1) ? make_float4(yx[cc][4 * q].y, yx[cc][4 * q + 1].y, yx[cc][4 * q + 2].y, yx[cc][4 * q + 3].y)
-                                      : make_float4(yx[cc][4 * q].x, yx[cc][4 * q + 1].x, yx[cc][4 * q + 2].x, yx[cc][4 * q + 3].x);
+                    if constexpr (I4) {   // the word's columns 0..3 are the pairs' x halves, 4..7 their y halves
+                        y4 = e4 ? make_float4(yx[cc][0].y, yx[cc][1].y, yx[cc][2].y, yx[cc][3].y)
+                                : make_float4(yx[cc][0].x, yx[cc][1].x, yx[cc][2].x, yx[cc][3].x);
                     } else {
                         y4 = make_float4(yr[cc][4 * e4], yr[cc][4 * e4 + 1], yr[cc][4 * e4 + 2], yr[cc][4 * e4 + 3]);
                     }
-                    reinterpret_cast<float4 *>(pq + (size_t)ci * VW)[e4] = y4;
+                    reinterpret_cast<float4 *>(pq + (size_t)ci * UW)[e4] = y4;
                 }
             }
             stamp(l, 5);
@@ -1254,17 +1244,26 @@ cudaError_t launch_stack_wt(int pdt, int kind, const StackArgs &a, int grid, siz
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kern, a);
     };
-    const int cpt = (a.d / Vec<WT>::N + STACK_NT - 1) / STACK_NT;
+    // units per thread of the FFN's mapping: 32-bit words (8 columns) for int4, else 16-byte chunks
+    const int cpt = (a.d / (WT == DT_INT4 ? 8 : Vec<WT>::N) + STACK_NT - 1) / STACK_NT;
     auto pick = [&](auto k1, auto k2, auto k3) -> cudaError_t {
         return cpt <= 1 ? go(k1) : (cpt == 2 ? go(k2) : (cpt == 3 ? go(k3) : cudaErrorNotSupported));
     };
     const bool gated = kind == KIND_GATED;
-    if constexpr (WT == DT_INT4) {
-        if (cpt != 1) return cudaErrorNotSupported;
+    if constexpr (WT == DT_INT4) {   // words per thread 2 (d <= 8192), 3 (d <= 12288), 4 (d <= 16384)
+        auto pick4 = [&](auto k2, auto k3, auto k4) -> cudaError_t {
+            return cpt <= 2 ? go(k2) : (cpt == 3 ? go(k3) : (cpt == 4 ? go(k4) : cudaErrorNotSupported));
+        };
         if (pdt == DT_F16)
-            return gated ? go(k_decode_stack<WT, DT_F16, KIND_GATED, 1>) : go(k_decode_stack<WT, DT_F16, KIND_RELU, 1>);
+            return gated ? pick4(k_decode_stack<WT, DT_F16, KIND_GATED, 2>, k_decode_stack<WT, DT_F16, KIND_GATED, 3>,
+                                 k_decode_stack<WT, DT_F16, KIND_GATED, 4>)
+                         : pick4(k_decode_stack<WT, DT_F16, KIND_RELU, 2>, k_decode_stack<WT, DT_F16, KIND_RELU, 3>,
+                                 k_decode_stack<WT, DT_F16, KIND_RELU, 4>);
         if (pdt == DT_BF16)
-            return gated ? go(k_decode_stack<WT, DT_BF16, KIND_GATED, 1>) : go(k_decode_stack<WT, DT_BF16, KIND_RELU, 1>);
+            return gated ? pick4(k_decode_stack<WT, DT_BF16, KIND_GATED, 2>, k_decode_stack<WT, DT_BF16, KIND_GATED, 3>,
+                                 k_decode_stack<WT, DT_BF16, KIND_GATED, 4>)
+                         : pick4(k_decode_stack<WT, DT_BF16, KIND_RELU, 2>, k_decode_stack<WT, DT_BF16, KIND_RELU, 3>,
+                                 k_decode_stack<WT, DT_BF16, KIND_RELU, 4>);
     } else {
         if (pdt == WT)
             return gated ? pick(k_decode_stack<WT, WT, KIND_GATED, 1>, k_decode_stack<WT, WT, KIND_GATED, 2>,

@@ -375,6 +375,26 @@ def test_decode_stack_three_chunks_per_thread(P, wi):
     ffn.close()
 
 
+@pytest.mark.parametrize("kind", ["relu", "gated"])
+@pytest.mark.parametrize("d", [8192, 12288, 16384])
+def test_decode_stack_int4_words_per_thread(P, d, kind):
+    """int4 rows: the FFN's threads take one 32-bit word (8 columns) at a time, 2, 3 and 4 words
+    of every row for d = 8192, 12288 and 16384; fc1/ReLU/fc2 and gated rows against the oracle."""
+    import dataclasses
+
+    w = dataclasses.replace(_wl(4, dict(d=d, f=3001, r=144), n_layers=2), kind=kind)
+    layers = build_layers(w, range(w.n_layers))
+    X = make_inputs(w, 2, 1, seed=41, device="cpu").numpy()
+    ffn = _handle(P, w, [g for g, _ in layers], stack_kernel=True)
+    P.pi_profile_begin(ffn.h)
+    ffn.decode_stack(to_dev(X[0]))
+    prof = P.pi_profile_end(ffn.h)
+    assert prof["decode_stack"][1] == 1, prof
+    _stack_vs_oracle(P, w, layers, X, ffn, ("int4", d, kind))
+    assert ffn.status() == 0
+    ffn.close()
+
+
 def test_grid_barrier_gives_up_cleanly(P):
     """A barrier that can never complete times out, reports PI_ERR_TIMEOUT, and the GPU stays usable."""
     work = torch.zeros(4, dtype=torch.int32, device="cuda")
