@@ -842,7 +842,11 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             }
             const int NPART = stage_parts<WT, KIND>(a);
             const int cq = lane * SNW + warp, cw = cq / NPART, cj = cq - cw * NPART;   // this thread's copy
-            if (nh + cw < nn && cw < SC) {
+            // Only the first batch's rows are requested now, the other free slots' rows once they
+            // have landed: requested together with everything else (every CTA asks for most of its
+            // rows at this point), the first rows land with the bulk of the layer's FFN bytes.
+            const int NF = nh == 0 ? max(1, min(4, SC / 2)) : SC;
+            if (nh + cw < nn && cw < SC && cw < NF) {
                 fence_proxy_async_smem();
                 uint32_t par;
                 stage_part<WT, KIND>(a, Lw, ring, mbar, slot_of(nh + cw, par), sneur[nh + cw], cj);
@@ -934,6 +938,13 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                         sls[k] = ring + (size_t)slot * a.slot_bytes;
                         got = got && mbar_wait(&mbar[slot], par);
                     }
+                }
+                // the held-back first copies (also after a timed-out wait: the give-up path below
+                // waits for every slot of the list's next SC entries)
+                if (bi == 0 && nh + cw < nn && cw >= NF && cw < SC) {
+                    fence_proxy_async_smem();
+                    uint32_t par;
+                    stage_part<WT, KIND>(a, Lw, ring, mbar, slot_of(nh + cw, par), sneur[nh + cw], cj);
                 }
                 if (got) {
                     constexpr int GI = KIND == KIND_GATED ? 2 : 1;
