@@ -715,13 +715,15 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             }
             if (tid == 0 && a.counts && nn) atomicAdd(a.counts + l, nn);
             __syncthreads();
-            if (a.balance > 1) {
-                // Within each group of G consecutive CTAs: every member publishes its list and an
-                // epoch (this launch and layer), waits for the other members' epochs, and takes an
-                // equal share (positions [r N / G, (r + 1) N / G) for member r) of the group's lists
-                // concatenated in member order. No grid barrier; the slowest member of a group has
-                // the mean of G counts instead of its own. Deterministic: fixed by the lists alone.
-                const int G = a.balance, g0 = c & ~(G - 1), rk = c - g0;
+            // Group balance, part 1 (a.balance = G > 1): within each group of G consecutive CTAs
+            // every member publishes its list and an epoch (this launch and layer); published
+            // after the first FFN copies instead, the fence and the flag round trips took
+            // microseconds longer behind the copies. A member keeps the first K0 entries of its own
+            // list, the first FFN batch, whose rows are requested at once; its share of the rest is
+            // settled while they land (part 2, below).
+            const int G = a.balance > 1 ? a.balance : 1;
+            const int K0 = max(1, min(4, S / 2));   // the first cold batch (no hot slots with balance)
+            if (G > 1) {
                 const unsigned long long epoch = s_base + (unsigned long long)(l + 1);
                 int32_t *gl = a.glist + (size_t)c * STACK_MAX_CHUNK;
                 for (int m = tid; m < nn; m += STACK_NT) gl[m] = sneur[m];
@@ -731,34 +733,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     __threadfence();
                     st_release_u64(a.gflag + c, epoch);
                 }
-                bool okw = true;
-                if (tid < G && tid != rk) okw = wait_flag_ge(a.gflag + g0 + tid, epoch);
-                if (!__syncthreads_and(okw)) {
-                    if (tid == 0) set_status(a.status, ST_TIMEOUT);
-                    return;
-                }
-                int *pref = reinterpret_cast<int *>(spb);   // [G + 1]; the logits' biases are dead now
-                if (tid == 0) {
-                    int run = 0;
-                    for (int q = 0; q < G; ++q) {
-                        pref[q] = run;
-                        run += __ldcg(a.gcount + g0 + q);
-                    }
-                    pref[G] = run;
-                }
-                __syncthreads();
-                const int N = pref[G];
-                const int lo = (int)((long long)rk * N / G);
-                nn = (int)((long long)(rk + 1) * N / G) - lo;
-                for (int m = tid; m < nn; m += STACK_NT) {
-                    const int q = lo + m;
-                    int a0 = 0;   // pref[a0] <= q < pref[a0 + 1]
-                    while (a0 + 1 < G && pref[a0 + 1] <= q) ++a0;
-                    const int i = __ldcg(a.glist + (size_t)(g0 + a0) * STACK_MAX_CHUNK + (q - pref[a0]));
-                    sneur[m] = i;
-                    if (!bias_bulk) sbias[m] = Lw.bg ? __ldg(Lw.bg + i) : 0.f;
-                }
-                __syncthreads();
+                nn = min(nn, K0);
             }
             if (a.balance == 1) {
                 // Every CTA publishes its list; after one more grid barrier each takes an equal share
@@ -860,9 +835,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     prefetch_line_l2((const char *)s_p2next + (size_t)(c + (size_t)P * k) * r * pb + 128 * (j % lines));
                 }
             }
-            // this thread's columns of u, scaled; int4: as fp32 pairs (i, i + 4) of its word's 8
-            // columns, the pairing of the decoded nibbles (i4_word_f32x2)
-            float ur[I4 ? 1 : CPT][I4 ? 1 : VW];
+            // this thread's columns of u, scaled, as fp32 pairs for the paired FMAs: int4 (i, i + 4)
+            // of its word's 8 columns, the pairing of the decoded nibbles (i4_word_f32x2); else
+            // (2j, 2j + 1) of its chunk
+            float2 ur[I4 ? 1 : CPT][I4 ? 1 : VW / 2];
             float2 ux[I4 ? CPT : 1][4];
 #pragma unroll
             for (int cc = 0; cc < CPT; ++cc) {
@@ -874,15 +850,13 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 } else {
 #pragma unroll
                     for (int e4 = 0; e4 < VW / 4; ++e4) {
-                        ur[cc][4 * e4 + 0] = xv[cc][e4].x * inv;
-                        ur[cc][4 * e4 + 1] = xv[cc][e4].y * inv;
-                        ur[cc][4 * e4 + 2] = xv[cc][e4].z * inv;
-                        ur[cc][4 * e4 + 3] = xv[cc][e4].w * inv;
+                        ur[cc][2 * e4 + 0] = make_float2(xv[cc][e4].x * inv, xv[cc][e4].y * inv);
+                        ur[cc][2 * e4 + 1] = make_float2(xv[cc][e4].z * inv, xv[cc][e4].w * inv);
                     }
                 }
             }
 
-            float yr[I4 ? 1 : CPT][I4 ? 1 : VW];
+            float2 yr[I4 ? 1 : CPT][I4 ? 1 : VW / 2];   // else: W_down sums as pairs (2j, 2j + 1)
             float2 yx[I4 ? CPT : 1][4];   // int4: W_down sums as pairs (i, i + 4) of the word's columns
 #pragma unroll
             for (int cc = 0; cc < CPT; ++cc) {
@@ -891,7 +865,75 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                     for (int j = 0; j < 4; ++j) yx[cc][j] = make_float2(0.f, 0.f);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < VW; ++e) yr[cc][e] = 0.f;
+                    for (int j = 0; j < VW / 2; ++j) yr[cc][j] = make_float2(0.f, 0.f);
+                }
+            }
+
+            if (G > 1) {
+                // Group balance, part 2: wait for the other members' epochs. Member q keeps
+                // L_q = min(n_q, K0) of its own entries; the rest of the group's lists (the pool,
+                // in member order) is dealt so that member q ends with T / G (+1 for q < T mod G)
+                // where it can: it takes pool positions [E_q, E_q + e_q), e_q = max(0, target_q - L_q),
+                // cut at the pool's end. The slowest member has about the mean of the G counts
+                // instead of its own. Deterministic: fixed by the lists alone.
+                const int g0 = c & ~(G - 1), rk = c - g0;
+                const unsigned long long epoch = s_base + (unsigned long long)(l + 1);
+                bool okw = true;
+                if (tid < G && tid != rk) okw = wait_flag_ge(a.gflag + g0 + tid, epoch);
+                if (!__syncthreads_and(okw)) {
+                    if (tid == 0) {   // wait (bounded) for the first batch's copies, then leave
+                        set_status(a.status, ST_TIMEOUT);
+                        for (int k = 0; k < nn && k < NF && k < SC; ++k) {
+                            uint32_t par;
+                            const int slot = slot_of(k, par);
+                            mbar_wait(&mbar[slot], par);
+                        }
+                    }
+                    return;
+                }
+                // pool prefix [G + 1], this member's range [2], the members' counts [G] (the logits'
+                // biases are dead now)
+                int *pp = reinterpret_cast<int *>(spb), *nq = pp + G + 3;
+                if (tid == 0) {
+                    int T = 0, run = 0;
+                    for (int q = 0; q < G; ++q) {
+                        nq[q] = __ldcg(a.gcount + g0 + q);
+                        T += nq[q];
+                    }
+                    for (int q = 0; q < G; ++q) {
+                        pp[q] = run;
+                        run += nq[q] - min(nq[q], K0);
+                    }
+                    pp[G] = run;
+                    int E = 0, myE = 0, mye = 0;
+                    for (int q = 0; q < G; ++q) {
+                        const int eq = max(0, T / G + (q < T % G ? 1 : 0) - min(nq[q], K0));
+                        if (q == rk) {
+                            myE = E;
+                            mye = eq;
+                        }
+                        E += eq;
+                    }
+                    pp[G + 1] = myE;
+                    pp[G + 2] = max(0, min(myE + mye, run) - myE);
+                }
+                __syncthreads();
+                const int E0 = pp[G + 1], ne = pp[G + 2];
+                for (int m = tid; m < ne; m += STACK_NT) {
+                    const int q = E0 + m;
+                    int a0 = 0;   // pp[a0] <= q < pp[a0 + 1]
+                    while (a0 + 1 < G && pp[a0 + 1] <= q) ++a0;
+                    const int i = __ldcg(a.glist + (size_t)(g0 + a0) * STACK_MAX_CHUNK + K0 + (q - pp[a0]));
+                    sneur[nn + m] = i;
+                    if (!bias_bulk) sbias[nn + m] = Lw.bg ? __ldg(Lw.bg + i) : 0.f;
+                }
+                __syncthreads();
+                const int n0 = nn;
+                nn += ne;
+                if (cw >= n0 && cw < NF && cw < nn && cw < SC) {   // first-batch entries the own list left empty
+                    fence_proxy_async_smem();
+                    uint32_t par;
+                    stage_part<WT, KIND>(a, Lw, ring, mbar, slot_of(cw, par), sneur[cw], cj);
                 }
             }
 
@@ -981,10 +1023,12 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                                 for (int k = 0; k < NB; ++k)
                                     unpack<WT>(reinterpret_cast<const uint4 *>(sls[k] + g * rowb)[ci], wf[k]);
 #pragma unroll
-                                for (int e = 0; e < VW; ++e)
+                                for (int k = 0; k < NB; ++k) {   // paired chains (even, odd columns), added at the end
+                                    float2 t2 = make_float2(wf[k][0] * ur[cc][0].x, wf[k][1] * ur[cc][0].y);
 #pragma unroll
-                                    for (int k = 0; k < NB; ++k)
-                                        v[GI * k + g] = fmaf(wf[k][e], ur[cc][e], v[GI * k + g]);
+                                    for (int j = 1; j < VW / 2; ++j) t2 = ffma2(make_float2(wf[k][2 * j], wf[k][2 * j + 1]), ur[cc][j], t2);
+                                    v[GI * k + g] += t2.x + t2.y;
+                                }
                             }
                         }
                     }
@@ -1071,7 +1115,8 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                                 float wf[VW];
                                 unpack<WT>(w4[k], wf);
 #pragma unroll
-                                for (int e = 0; e < VW; ++e) yr[cc][e] = fmaf(hvb[k], wf[e], yr[cc][e]);
+                                for (int j = 0; j < VW / 2; ++j)
+                                    yr[cc][j] = ffma2(make_float2(hvb[k], hvb[k]), make_float2(wf[2 * j], wf[2 * j + 1]), yr[cc][j]);
                             }
                         }
                     }
@@ -1096,7 +1141,8 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                                 float wf[VW];
                                 unpack<WT>(reinterpret_cast<const uint4 *>(sl + (ROWS - 1) * rowb)[ci], wf);
 #pragma unroll
-                                for (int e = 0; e < VW; ++e) yr[cc][e] = fmaf(hvb[k], wf[e], yr[cc][e]);
+                                for (int j = 0; j < VW / 2; ++j)
+                                    yr[cc][j] = ffma2(make_float2(hvb[k], hvb[k]), make_float2(wf[2 * j], wf[2 * j + 1]), yr[cc][j]);
                             }
                         }
                     }
@@ -1123,7 +1169,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                         y4 = e4 ? make_float4(yx[cc][0].y, yx[cc][1].y, yx[cc][2].y, yx[cc][3].y)
                                 : make_float4(yx[cc][0].x, yx[cc][1].x, yx[cc][2].x, yx[cc][3].x);
                     } else {
-                        y4 = make_float4(yr[cc][4 * e4], yr[cc][4 * e4 + 1], yr[cc][4 * e4 + 2], yr[cc][4 * e4 + 3]);
+                        y4 = make_float4(yr[cc][2 * e4].x, yr[cc][2 * e4].y, yr[cc][2 * e4 + 1].x, yr[cc][2 * e4 + 1].y);
                     }
                     reinterpret_cast<float4 *>(pq + (size_t)ci * UW)[e4] = y4;
                 }
