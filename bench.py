@@ -56,9 +56,9 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # first 4 layers: dram__bytes_read.sum + dram__bytes_write.sum, mean of two launches
-    # (608.837120 + 22.827776 MB and 613.342464 + 19.888640 MB)
+    # (608.808960 + 23.127808 MB and 613.347584 + 20.167424 MB)
     ("opt175b_d12288_f49152_int4_L96", "decode_stack"): {
-        "bytes_per_layer": (608837120 + 22827776 + 613342464 + 19888640) / 2 / 4, "csrc": "c15ca7f4033f56d0"},
+        "bytes_per_layer": (608808960 + 23127808 + 613347584 + 20167424) / 2 / 4, "csrc": "402e98d303381201"},
 }
 
 
