@@ -42,7 +42,7 @@ PI_STACK_PHASES = 8
 STACK_PHASE_NAMES = ("layer_start", "hidden_done", "logits_start", "list_ready", "first_rows", "ffn_done",
                      "reduce_start", "reduce_done")
 PI_NOALLOC_SCRATCH_BYTES = 16 << 20
-KERNEL_KINDS = ("rms", "pred_hidden", "pred_logits", "ffn_h", "ffn_down", "reduce", "decode_stack")
+KERNEL_KINDS = ("rms", "pred_hidden", "pred_logits", "ffn_h", "ffn_down", "reduce", "decode_stack", "pred_fused")
 
 
 class PiFfnDesc(ctypes.Structure):

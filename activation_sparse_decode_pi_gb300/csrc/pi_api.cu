@@ -193,6 +193,8 @@ struct pi_ffn {
     int stack_pf = 1;                  // L2 prefetch of the persistent step: bit 0 P1, bit 1 unstaged P2 rows (PI_FFN_STACK_PF)
     int stack_pf_frac = 256;           // share (of 256) of the unstaged P2 rows prefetched during the FFN (PI_FFN_STACK_PF_P2_FRAC)
     int off_ring = 0, off_flags = 0, off_mbar = 0, off_hp = 0, off_scr = 0, stack_ring = 0;
+    // fused predictor for batches up to pf_maxb (set by plan_pred_fused)
+    int pf_maxb = 0;
     // tensor-core path (batch >= tc_min_b, set by plan_tc)
     bool tc_ok = false;
     int tc_min_b = 16, tc_nbmax = 0, tc_rpad = 0, tc_fpad = 0;
@@ -262,10 +264,55 @@ struct ProfScope {
     }
 };
 
+// A positive integer from the environment, else def.
+int env_int(const char *name, int def)
+{
+    const char *v = std::getenv(name);
+    return v && std::atoi(v) > 0 ? std::atoi(v) : def;
+}
+
+// Whether the fused predictor serves batch B on this handle.
+bool pf_use(const pi_ffn_t *h, int B) { return B >= 1 && B <= h->pf_maxb; }
+
+// The fused predictor (K1 + K2 in one cooperative launch) for one layer: u = x * inv_rms (inv_rms
+// per row when given, else computed from x when rms_self, else u = x).
+cudaError_t fused_predict(const pi_ffn_t *h, int layer, const float *x, const float *inv_rms, int rms_self, int B,
+                          int32_t *idx, int32_t *count, cudaStream_t s)
+{
+    const pi_ffn_desc_t &D = h->desc;
+    const pi_layer_weights_t &w = h->layers[layer];
+    FusedPredArgs a;
+    a.p1t = w.p1_t;
+    a.p2t = w.p2_t;
+    a.b_pred = w.b_pred;
+    a.d = D.d;
+    a.r = D.r;
+    a.f = D.f;
+    a.B = B;
+    a.hot = h->hot_prefix;
+    a.rms_self = rms_self;
+    a.tau = D.tau_logit;
+    a.eps = RMS_EPS;
+    a.x = x;
+    a.inv_rms = inv_rms;
+    a.hp = h->hp;
+    a.maskw = h->maskw;
+    a.ticket = h->tickets + 0;
+    a.status = h->status;
+    a.bar = reinterpret_cast<unsigned long long *>(h->tickets + 4);
+    a.idx = idx;
+    a.count = count;
+    const int bt = B <= 2 ? 2 : (B <= 4 ? 4 : 8);
+    const size_t smem = (size_t)B * std::max(D.d, D.r) * 4;
+    ProfScope p(h, s, PI_K_PRED_FUSED);
+    return launch_pred_fused(D.pdtype, bt, a, h->nsm, smem, s);
+}
+
 // K1 + K2 for one layer. pdl_first: whether the first kernel may overlap its predecessor.
 cudaError_t enqueue_predict(const pi_ffn_t *h, int layer, const float *x, const float *inv_rms, int B,
                             int32_t *idx, int32_t *count, cudaStream_t s, bool pdl_first)
 {
+    if (pf_use(h, B)) return fused_predict(h, layer, x, inv_rms, 0, B, idx, count, s);
     const pi_ffn_desc_t &D = h->desc;
     const pi_layer_weights_t &w = h->layers[layer];
     const int bt1 = pick_bt(B, D.d), bt2 = pick_bt(B, D.r);
@@ -346,10 +393,6 @@ void plan_tc(pi_ffn_t *h)
         cudaGetLastError();
         return;
     }
-    auto env_int = [](const char *name, int def) {
-        const char *v = std::getenv(name);
-        return v && std::atoi(v) > 0 ? std::atoi(v) : def;
-    };
     h->tc_kw = env_int("PI_FFN_TC_KW", 2) >= 2 ? 2 : 1;
     h->tc_ds = env_int("PI_FFN_TC_DS", 2) >= 2 ? 2 : 1;
     h->tc_hidden_cpt = std::max(1, env_int("PI_FFN_TC_HIDDEN_CPT", 8));
@@ -566,7 +609,9 @@ cudaError_t enqueue_stack_tc(const pi_ffn_t *h, const float *x0, int B, float *x
         int32_t *idx = idx_out ? idx_out + (size_t)l * D.f : h->idx_ws;
         int32_t *cnt = counts ? counts + l : h->counts_ws + l;
         if ((e = tc_split(h, xl, B, 1, s, l > 0)) != cudaSuccess) return e;
-        if ((e = tc_predict(h, l, B, idx, cnt, s)) != cudaSuccess) return e;
+        if ((e = pf_use(h, B) ? fused_predict(h, l, xl, nullptr, 1, B, idx, cnt, s) : tc_predict(h, l, B, idx, cnt, s)) !=
+            cudaSuccess)
+            return e;
         if ((e = tc_ffn(h, l, B, idx, cnt, xl, xn, s)) != cudaSuccess) return e;
         xl = xn;
     }
@@ -597,6 +642,34 @@ cudaError_t enqueue_stack(const pi_ffn_t *h, const float *x0, int B, float *x_ou
 }
 
 bool legacy_stream(cudaStream_t s) { return s == nullptr || s == cudaStreamLegacy; }
+
+// The largest batch the fused predictor serves on this handle (0: none): its shared memory holds
+// B rows of max(d, r) floats, each CTA at most FP_MAX_WORDS mask words. Off unless
+// PI_FFN_PRED_FUSED=1 in the environment: measured on a GB300 it is slower than the two
+// predictor kernels at batches 1-8 (those overlap their weight loads with the previous kernel
+// through programmatic dependent launch; a cooperative launch cannot). PI_FFN_PRED_FUSED_MAXB
+// lowers its batch bound (default 8).
+void plan_pred_fused(pi_ffn_t *h)
+{
+    h->pf_maxb = 0;
+    const char *env = std::getenv("PI_FFN_PRED_FUSED");
+    if (!env || env[0] != '1') return;
+    const pi_ffn_desc_t &D = h->desc;
+    if (D.pdtype != PI_F32 && D.pdtype != PI_BF16 && D.pdtype != PI_F16) return;
+    const int V = D.pdtype == PI_F32 ? 4 : 8;
+    if (D.d % V || D.r % V) return;
+    const int W = (D.f + 31) / 32;
+    if ((W + h->nsm - 1) / h->nsm > FP_MAX_WORDS) return;
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    const long long row = (long long)std::max(D.d, D.r) * 4;
+    const long long fit = (optin - 8 * 1024) / row;   // static shared memory and slack
+    h->pf_maxb = (int)std::min<long long>({8, fit, (long long)D.max_batch, (long long)env_int("PI_FFN_PRED_FUSED_MAXB", 8)});
+    if (h->pf_maxb < 1) h->pf_maxb = 0;
+}
 
 // Whether the persistent decode-step kernel serves this handle at batch 1, and its
 // shared-memory layout. PI_FFN_STACK_KERNEL=0 in the environment turns it off.
@@ -786,6 +859,7 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
     }
 
     plan_tc(h);
+    plan_pred_fused(h);
     const pi_ffn_desc_t &D = h->desc;
     const size_t mb = (size_t)D.max_batch;
     const size_t tnb = h->tc_ok ? (size_t)h->tc_nbmax : 0;
@@ -798,7 +872,7 @@ pi_status_t pi_ffn_create(pi_ffn_t **out, const pi_ffn_desc_t *desc, const pi_la
         mb * D.f * 4,                                  // hbuf
         (size_t)MAX_GROUPS * mb * D.d * 4,             // part
         (size_t)(D.f + 31) / 32 * 4,                   // maskw
-        4 * 4,                                         // tickets
+        8 * 4,                                         // tickets: [0] logits, [1] reduce, [2..3] stack barrier, [4..5] fused predictor barrier
         4,                                             // status
         (size_t)D.f * 4,                               // idx_ws
         4,                                             // count_ws
@@ -902,7 +976,7 @@ pi_status_t pi_predict(pi_ffn_t *h, int32_t layer, const float *u, int32_t B, in
     if ((s = check_ptr(u, (size_t)B * D.d * 4, 16, h->dev))) return s;
     if ((s = check_ptr(idx, (size_t)D.f * 4, 4, h->dev))) return s;
     if ((s = check_ptr(count, 4, 4, h->dev))) return s;
-    if (tc_use(h, B)) {
+    if (tc_use(h, B) && !pf_use(h, B)) {
         cudaError_t e = tc_split(h, u, B, 0, (cudaStream_t)stream, false);
         if (e == cudaSuccess) e = tc_predict(h, layer, B, idx, count, (cudaStream_t)stream);
         return cuda_status(e);
@@ -1077,8 +1151,9 @@ pi_status_t pi_get_status(pi_ffn_t *h)
     uint32_t v = 0;
     if (cudaMemcpy(&v, h->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_status(cudaGetLastError());
     if (v && cudaMemset(h->status, 0, 4) != cudaSuccess) return cuda_status(cudaGetLastError());
-    // a grid barrier that gave up leaves its arrival count behind: start the next step clean
-    if (v == PI_ERR_TIMEOUT && cudaMemset(h->tickets + 2, 0, 8) != cudaSuccess) return cuda_status(cudaGetLastError());
+    // a grid barrier that gave up leaves its arrival count (and the compaction ticket behind it)
+    // behind: start the next step clean
+    if (v == PI_ERR_TIMEOUT && cudaMemset(h->tickets, 0, 8 * 4) != cudaSuccess) return cuda_status(cudaGetLastError());
     // the group exchange's epochs derive from the barrier counter: restart them with it
     if (v == PI_ERR_TIMEOUT && h->stack_gflag && cudaMemset(h->stack_gflag, 0, (size_t)h->nsm * 8) != cudaSuccess)
         return cuda_status(cudaGetLastError());

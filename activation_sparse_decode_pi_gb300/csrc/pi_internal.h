@@ -171,6 +171,27 @@ cudaError_t launch_pred_logits(const Launch &L, int pdt, int bt, const void *p2t
                                const float *b_pred, float tau, const float *hp, int B,
                                uint32_t *maskw, uint32_t *ticket, int32_t *idx, int32_t *count, int hot);
 
+// Fused predictor for small batches (one cooperative launch per layer, grid = one CTA per SM):
+// hp = max(0, inv_rms_b * (P1T . x_b)) over all CTAs, one bounded grid barrier, then the logits
+// and union mask of 32-neuron words (a contiguous range of words per CTA) and the compaction
+// of the mask by the last CTA (as K1 + K2). inv_rms: given per row, or computed here from x
+// (rms_self), or neither (x is u). hp is [B x r] workspace; bar a 64-bit grid-barrier counter
+// of its own; ticket 0 on entry (left 0).
+constexpr int FP_NT = 512;              // threads per CTA of the fused predictor
+constexpr int FP_MAX_WORDS = 64;        // mask words per CTA (f <= 2048 * grid)
+struct FusedPredArgs {
+    const void *p1t, *p2t;
+    const float *b_pred;
+    int d, r, f, B, hot, rms_self;
+    float tau, eps;
+    const float *x, *inv_rms;
+    float *hp;
+    uint32_t *maskw, *ticket, *status;
+    unsigned long long *bar;
+    int32_t *idx, *count;
+};
+cudaError_t launch_pred_fused(int pdt, int bt, const FusedPredArgs &a, int grid, size_t smem, cudaStream_t s);
+
 // K3: h[b,j] for the listed neurons j < *count.
 cudaError_t launch_ffn_h(const Launch &L, int wdt, int kind, int bt, const void *wg, const void *wu,
                          const void *sg, const void *su, const float *bg, int d, int f,

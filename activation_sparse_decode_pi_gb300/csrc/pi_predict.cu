@@ -10,6 +10,7 @@
 // Both are HBM-bound streams of the predictor weights. The weight loads of the
 // first chunk batch are issued before waiting for the producer of u / hp
 // (programmatic dependent launch), so they overlap the previous kernel's tail.
+#include "pi_async.cuh"
 #include "pi_common.cuh"
 #include "pi_internal.h"
 #include "pi_rowdot.cuh"
@@ -157,6 +158,193 @@ k_pred_logits(const uint4 *__restrict__ P2, int r, int f, const float *__restric
     if (threadIdx.x == 0) *ticket = 0u;
 }
 
+// ---------------------------------------------------------------- fused predictor ------------
+// Small batches: K1 and K2 as one cooperative launch over every SM. Each CTA stages the B input
+// rows in shared memory, takes r / grid rows of P1 (thread t: chunks t, t + 512, ... of RG rows
+// at once, the rows' dot products with every input row), and after one bounded grid barrier
+// the logits of a contiguous range of 32-neuron mask words: warp w takes NPW neurons at a time,
+// all their P2 chunks in flight, and the union over the rows sets the neuron's bit. The last
+// CTA to finish compacts the mask words into the ascending list.
+template <int PT, int BT>
+__global__ void __launch_bounds__(FP_NT, 1) k_pred_fused(FusedPredArgs a)
+{
+    constexpr int V = Vec<PT>::N, FW = FP_NT / 32;
+    constexpr int RG = BT >= 4 ? 32 / BT : 8;   // P1 rows per pass: RG * BT <= 32 sums per thread
+    constexpr int NPW = BT <= 4 ? 3 : 2;        // neurons per warp in flight in the logits
+    constexpr int QC = 4;                       // P2 chunks per lane and neuron in flight
+    extern __shared__ float4 fsm4[];
+    float *xs = reinterpret_cast<float *>(fsm4);   // [B][d] the inputs, then [B][r] hp
+    __shared__ float red[FW][32];
+    __shared__ float sinv[BT];
+    __shared__ uint32_t sword[FP_MAX_WORDS];
+    __shared__ unsigned long long s_base;
+    __shared__ int s_flag, wsum[FW];
+    __shared__ bool s_last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = gridDim.x, c = blockIdx.x, B = a.B, d = a.d, r = a.r, f = a.f;
+    if (tid == 0) s_base = barrier_base(a.bar, (unsigned long long)P);
+
+    // the input rows into shared memory, and their RMS scales
+    float ssq[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+        ssq[b] = 0.f;
+        if (b < B)
+            for (int j = tid; j < d / 4; j += FP_NT) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.x + (size_t)b * d) + j);
+                reinterpret_cast<float4 *>(xs + (size_t)b * d)[j] = v;
+                ssq[b] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            }
+    }
+    if (a.rms_self) {
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+            const float t = warp_sum(ssq[b]);
+            if (lane == 0) red[warp][b] = t;
+        }
+        __syncthreads();
+        if (tid < BT) {
+            float t = 0.f;
+            for (int w = 0; w < FW; ++w) t += red[w][tid];   // fixed order
+            sinv[tid] = 1.f / sqrtf(t / (float)d + a.eps);
+        }
+    } else if (tid < BT) {
+        sinv[tid] = (a.inv_rms && tid < B) ? a.inv_rms[tid] : 1.f;
+    }
+    __syncthreads();
+
+    // hidden layer: rows [k0, k1) of P1T
+    const int k0 = (int)((long long)c * r / P), k1 = (int)((long long)(c + 1) * r / P);
+    const int nch = d / V;
+    const uint4 *p1 = reinterpret_cast<const uint4 *>(a.p1t);
+    for (int kb = k0; kb < k1; kb += RG) {
+        float acc[RG][BT];
+#pragma unroll
+        for (int g = 0; g < RG; ++g)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) acc[g][b] = 0.f;
+        for (int j = tid; j < nch; j += FP_NT) {
+            uint4 wv[RG];
+#pragma unroll
+            for (int g = 0; g < RG; ++g)
+                wv[g] = kb + g < k1 ? __ldg(p1 + (size_t)(kb + g) * nch + j) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+                if (b >= B) break;
+                float xv[V];
+#pragma unroll
+                for (int e4 = 0; e4 < V / 4; ++e4) {
+                    const float4 t = reinterpret_cast<const float4 *>(xs + (size_t)b * d + (size_t)j * V)[e4];
+                    xv[4 * e4] = t.x; xv[4 * e4 + 1] = t.y; xv[4 * e4 + 2] = t.z; xv[4 * e4 + 3] = t.w;
+                }
+#pragma unroll
+                for (int g = 0; g < RG; ++g) {
+                    float wf[V];
+                    unpack<PT>(wv[g], wf);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) acc[g][b] = fmaf(wf[e], xv[e], acc[g][b]);
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < RG; ++g)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+                const float t = warp_sum(acc[g][b]);
+                if (lane == 0) red[warp][g * BT + b] = t;
+            }
+        __syncthreads();
+        if (tid < RG * BT) {
+            const int g = tid / BT, b = tid - g * BT;
+            float t = 0.f;
+            for (int w = 0; w < FW; ++w) t += red[w][tid];   // fixed order
+            if (kb + g < k1 && b < B) a.hp[(size_t)b * r + kb + g] = fmaxf(t * sinv[b], 0.f);
+        }
+        __syncthreads();
+    }
+    if (!grid_sync_to(a.bar, s_base + (unsigned long long)P, a.status, &s_flag)) return;
+
+    // logits of the words [w0, w1): hp into shared memory first
+    float *hs = xs;
+#pragma unroll
+    for (int b = 0; b < BT; ++b)
+        if (b < B)
+            for (int j = tid; j < r / 4; j += FP_NT)
+                reinterpret_cast<float4 *>(hs + (size_t)b * r)[j] = __ldcg(reinterpret_cast<const float4 *>(a.hp + (size_t)b * r) + j);
+    const int W = (f + 31) / 32;
+    const int w0 = (int)((long long)c * W / P), w1 = (int)((long long)(c + 1) * W / P);
+    for (int i = tid; i < w1 - w0; i += FP_NT) sword[i] = 0u;
+    __syncthreads();
+    const int n0 = 32 * w0, n1 = min(f, 32 * w1), nchr = r / V;
+    const uint4 *p2 = reinterpret_cast<const uint4 *>(a.p2t);
+    for (int nb = n0 + warp * NPW; nb < n1; nb += FW * NPW) {
+        float acc[NPW][BT];
+#pragma unroll
+        for (int p = 0; p < NPW; ++p)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) acc[p][b] = 0.f;
+        for (int q0 = lane; q0 < nchr; q0 += 32 * QC) {
+            uint4 wv[NPW][QC];
+#pragma unroll
+            for (int p = 0; p < NPW; ++p) {
+                const int i = nb + p;
+                const bool need = i < n1 && i >= a.hot;   // the hot prefix needs no logit
+#pragma unroll
+                for (int u = 0; u < QC; ++u) {
+                    const int q = q0 + 32 * u;
+                    wv[p][u] = need && q < nchr ? __ldg(p2 + (size_t)i * nchr + q) : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < QC; ++u) {
+                const int q = q0 + 32 * u;
+                if (q >= nchr) break;
+#pragma unroll
+                for (int b = 0; b < BT; ++b) {
+                    if (b >= B) break;
+                    float hv[V];
+#pragma unroll
+                    for (int e4 = 0; e4 < V / 4; ++e4) {
+                        const float4 t = reinterpret_cast<const float4 *>(hs + (size_t)b * r + (size_t)q * V)[e4];
+                        hv[4 * e4] = t.x; hv[4 * e4 + 1] = t.y; hv[4 * e4 + 2] = t.z; hv[4 * e4 + 3] = t.w;
+                    }
+#pragma unroll
+                    for (int p = 0; p < NPW; ++p) {
+                        float wf[V];
+                        unpack<PT>(wv[p][u], wf);
+#pragma unroll
+                        for (int e = 0; e < V; ++e) acc[p][b] = fmaf(wf[e], hv[e], acc[p][b]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < NPW; ++p) {
+            const int i = nb + p;
+            const float bias = (i < n1 && a.b_pred) ? __ldg(a.b_pred + i) : 0.f;
+            bool act = false;
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+                const float z = warp_sum(acc[p][b]) + bias;
+                act = act || (b < B && z > a.tau);
+            }
+            if (lane == 0 && i < n1 && (i < a.hot || act)) atomicOr(&sword[(i >> 5) - w0], 1u << (i & 31));
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < w1 - w0; i += FP_NT) a.maskw[w0 + i] = sword[i];
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        s_last = atomicAdd(a.ticket, 1u) == (unsigned)P - 1u;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    compact_words<FW>(a.maskw, W, 0, a.idx, a.count, wsum, [] { __syncthreads(); });
+    if (tid == 0) *a.ticket = 0u;
+}
+
 // ---------------------------------------------------------------- launchers ------------------
 
 template <int PT>
@@ -215,6 +403,46 @@ cudaError_t launch_pred_logits(const Launch &L, int pdt, int bt, const void *p2t
     case DT_F32: return logits_bt<DT_F32>(L, bt, p2t, r, f, b_pred, tau, hp, B, maskw, ticket, idx, count, hot);
     case DT_BF16: return logits_bt<DT_BF16>(L, bt, p2t, r, f, b_pred, tau, hp, B, maskw, ticket, idx, count, hot);
     case DT_F16: return logits_bt<DT_F16>(L, bt, p2t, r, f, b_pred, tau, hp, B, maskw, ticket, idx, count, hot);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int PT>
+static cudaError_t fused_bt(int bt, const FusedPredArgs &a, int grid, size_t smem, cudaStream_t s)
+{
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, FP_NT, smem);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorNotSupported;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(FP_NT);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, a);
+    };
+    switch (bt) {
+    case 2: return go(k_pred_fused<PT, 2>);
+    case 4: return go(k_pred_fused<PT, 4>);
+    case 8: return go(k_pred_fused<PT, 8>);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pred_fused(int pdt, int bt, const FusedPredArgs &a, int grid, size_t smem, cudaStream_t s)
+{
+    switch (pdt) {
+    case DT_F32: return fused_bt<DT_F32>(bt, a, grid, smem, s);
+    case DT_BF16: return fused_bt<DT_BF16>(bt, a, grid, smem, s);
+    case DT_F16: return fused_bt<DT_F16>(bt, a, grid, smem, s);
     }
     return cudaErrorInvalidValue;
 }

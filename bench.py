@@ -154,6 +154,8 @@ def kernel_bytes(w, kind: str, count: float, B: int, counts_per_layer=None, hot:
         return w.r * w.d * pb
     if kind == "pred_logits":
         return (w.f - hot) * w.r * pb + w.f * 4
+    if kind == "pred_fused":   # hidden layer + logits in one launch
+        return w.r * w.d * pb + (w.f - hot) * w.r * pb + w.f * 4
     if kind == "ffn_h":
         rows = 2 if w.kind == "gated" else 1
         return count * (rows * (w.d * wb + sc) + 4)
@@ -509,8 +511,10 @@ def run_ours(args):
         "bytes_per_step": bytes_per_step,
         "mean_active_per_layer": mean_count,
         "predictor_byte_share": predictor_bytes(w, hot_prefix) * w.n_layers / bytes_per_step if bytes_per_step else None,
-        "predictor_time_share": ((kinds.get("pred_hidden", (0.0, 0))[0] + kinds.get("pred_logits", (0.0, 0))[0]) /
-                                 sum(v[0] for v in kinds.values())) if ("pred_hidden" in kinds) else None,
+        "predictor_time_share": ((kinds.get("pred_hidden", (0.0, 0))[0] + kinds.get("pred_logits", (0.0, 0))[0] +
+                                  kinds.get("pred_fused", (0.0, 0))[0]) /
+                                 sum(v[0] for v in kinds.values()))
+                                if ("pred_hidden" in kinds or "pred_fused" in kinds) else None,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w, dom, B, hot_prefix, n_hot), "algorithmic_bytes": dom_bytes,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"

@@ -51,6 +51,12 @@
  *  - PI_FFN_TC=0            every batch > 1 stays on the CUDA-core kernels.
  *  - PI_FFN_TC_MIN_BATCH=n  smallest batch for the tensor-core path (default 3 for
  *                           d >= 5120, else 6).
+ *  - PI_FFN_PRED_FUSED=1    the predictor of batches up to 8 (pi_predict, the multi-kernel and
+ *                           tensor-core steps) runs as one cooperative launch (hidden layer over
+ *                           all SMs, a grid barrier, logits, mask and compaction) instead of two
+ *                           kernels; off by default (slower on a GB300, see the design notes).
+ *  - PI_FFN_PRED_FUSED_MAXB=n  largest batch for the one-launch predictor (default 8; also
+ *                           bounded by B * max(d, r) * 4 bytes of shared memory).
  *  - PI_FFN_TC_KW, PI_FFN_TC_DS, PI_FFN_TC_STAGES, PI_FFN_TC_HIDDEN_CPT: tensor-core step
  *    widths (64-wide K blocks per step, 128-column W_down slices per tile: 1 or 2, default
  *    2), ring depth cap, and CTAs per predictor-hidden tile (default 8).
@@ -249,7 +255,8 @@ typedef enum {
     PI_K_FFN_DOWN = 4,     /* row-sparse W_down axpy into fp32 partials */
     PI_K_REDUCE = 5,       /* deterministic reduction (+ residual, next RMS scale) */
     PI_K_STACK = 6,        /* persistent decode step, all layers in one kernel (batch 1) */
-    PI_K_COUNT = 7
+    PI_K_PRED_FUSED = 7,   /* predictor hidden layer + logits + union mask + compaction, one launch (small batches) */
+    PI_K_COUNT = 8
 } pi_kernel_kind_t;
 
 pi_status_t pi_profile_begin(pi_ffn_t *h);

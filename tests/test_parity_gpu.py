@@ -85,6 +85,37 @@ def test_predict_small(P, wi, B):
     ffn.close()
 
 
+@pytest.mark.parametrize("B", [1, 2, 5, 8])
+@pytest.mark.parametrize("wi", range(5))
+def test_predict_fused_vs_two_kernels(P, wi, B):
+    """The optional one-launch predictor of batches up to 8 (PI_FFN_PRED_FUSED=1: hidden layer over
+    all SMs, a grid barrier, logits of contiguous mask words, compaction by the last CTA): against
+    the oracle, and the same list as the two-kernel predictor outside the threshold band."""
+    w = _wl(wi, MID)
+    (Lg, Lo), = build_layers(w, [0])
+    u = rms_inputs(w, B, seed=11 + B)[0]
+    pr = oracle.predict(u.astype(np.float64), Lo["p1_t"], Lo["p2_t"], Lo["b_pred"], w.pdtype)
+    lists = {}
+    for fused in ("1", "0"):
+        ffn = _with_env("PI_FFN_PRED_FUSED", fused, lambda: P.SparseFFN.from_workload(w, [Lg], max_batch=B))
+        P.pi_profile_begin(ffn.h)
+        idx, cnt = ffn.predict(0, to_dev(u))
+        prof = P.pi_profile_end(ffn.h)
+        assert (prof["pred_fused"][1] == 1) == (fused == "1"), prof
+        n = int(cnt.item())
+        gi = idx[:n].cpu().numpy()
+        assert np.all(np.diff(gi) > 0), "active list must be ascending and unique"
+        diff = np.setxor1d(gi, pr["idx"])
+        assert np.all(band_mask(pr["z"])[diff]), (fused, f"{diff.size} out-of-band mismatches")
+        idx2, cnt2 = ffn.predict(0, to_dev(u))
+        assert int(cnt2.item()) == n and torch.equal(idx2[:n], idx[:n]), "predictor is not deterministic"
+        assert ffn.status() == 0
+        lists[fused] = gi
+        ffn.close()
+    diff = np.setxor1d(lists["1"], lists["0"])
+    assert np.all(band_mask(pr["z"])[diff])
+
+
 # ------------------------------------------------------------------ sparse FFN ----------------
 
 def _lists(rng, f, pred_idx):

@@ -86,7 +86,8 @@ def _env(**kv):
 
 
 def _handle(P, w, layers, B, min_batch=None):
-    with _env(PI_FFN_TC="1", PI_FFN_TC_MIN_BATCH=None if min_batch is None else str(min_batch)):
+    # the tensor-core predictor too (not the optional one-launch predictor of small batches)
+    with _env(PI_FFN_TC="1", PI_FFN_PRED_FUSED="0", PI_FFN_TC_MIN_BATCH=None if min_batch is None else str(min_batch)):
         return P.SparseFFN.from_workload(w, layers, max_batch=B)
 
 
