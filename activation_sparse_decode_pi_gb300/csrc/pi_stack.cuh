@@ -716,9 +716,10 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             if (tid == 0 && a.counts && nn) atomicAdd(a.counts + l, nn);
             __syncthreads();
             // Group balance, part 1 (a.balance = G > 1): within each group of G consecutive CTAs
-            // every member publishes its list and an epoch (this launch and layer); published
-            // after the first FFN copies instead, the fence and the flag round trips took
-            // microseconds longer behind the copies. A member keeps the first K0 entries of its own
+            // every member publishes its list and an epoch (this launch and layer) with a release
+            // store after the CTA barrier (a fence before it cost ~2 µs under the logits' copy
+            // traffic; published after the first FFN copies, the flag round trips took microseconds
+            // longer behind them). A member keeps the first K0 entries of its own
             // list, the first FFN batch, whose rows are requested at once; its share of the rest is
             // settled while they land (part 2, below).
             const int G = a.balance > 1 ? a.balance : 1;
@@ -729,10 +730,7 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
                 for (int m = tid; m < nn; m += STACK_NT) gl[m] = sneur[m];
                 if (tid == 0) a.gcount[c] = nn;
                 __syncthreads();   // the CTA's list stores come before the release below
-                if (tid == 0) {
-                    __threadfence();
-                    st_release_u64(a.gflag + c, epoch);
-                }
+                if (tid == 0) st_release_u64(a.gflag + c, epoch);   // release: the CTA's writes before the CTA barrier
                 nn = min(nn, K0);
             }
             if (a.balance == 1) {
