@@ -38,10 +38,10 @@
  *  - PI_FFN_STACK_BALANCE=n the persistent step spreads the layer's active neurons evenly: 1
  *                           over all CTAs (one more grid barrier per layer), 2, 4 or 8 within
  *                           groups of as many consecutive CTAs (the members exchange their lists
- *                           through memory, no grid barrier); 0 (the default): each CTA computes
- *                           its own active neurons. Groups of 8 are ~7% faster on Llama2-13B-like
- *                           gated bf16 layers (d 5120), slower on the OPT-175B- and ReluLLaMA-7B-like
- *                           ones.
+ *                           through memory, no grid barrier); 0: each CTA computes its own active
+ *                           neurons. Default 8 for gated 16-bit layers with d >= 5120 (~7% faster
+ *                           on Llama2-13B-like layers), else 0 (slower on the OPT-175B- and
+ *                           ReluLLaMA-7B-like ones).
  *  - PI_FFN_STACK_PF=n      L2 prefetches of the persistent step, a bit mask: 1 = the next
  *                           layer's P1 rows (during the grid barrier after the FFN, or a whole
  *                           layer ahead with 4), 2 = the next layer's P2 rows that the ring does
