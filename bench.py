@@ -56,9 +56,9 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # first 4 layers: dram__bytes_read.sum + dram__bytes_write.sum, mean of two launches
-    # (608.808192 + 23.075328 MB and 613.348864 + 20.076544 MB)
+    # (608.862720 + 23.151872 MB and 613.509120 + 20.072448 MB)
     ("opt175b_d12288_f49152_int4_L96", "decode_stack"): {
-        "bytes_per_layer": (608808192 + 23075328 + 613348864 + 20076544) / 2 / 4, "csrc": "71c35bd808ccc18b"},
+        "bytes_per_layer": (608862720 + 23151872 + 613509120 + 20072448) / 2 / 4, "csrc": "990bc25d717e68c9"},
 }
 
 
