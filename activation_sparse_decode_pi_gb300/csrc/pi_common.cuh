@@ -53,6 +53,16 @@ __device__ __forceinline__ void pdl_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Last-CTA ticket: one acquire-release atomic instead of fence + atomic + fence. The release
+// publishes this CTA's stores (made before the caller's CTA barrier); the CTA that draws the last
+// ticket acquires everyone else's (its other threads after the next CTA barrier).
+__device__ __forceinline__ uint32_t ticket_acq_rel(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void set_status(uint32_t *status, uint32_t code)
 {
     if (status) atomicCAS(status, 0u, code);

@@ -291,13 +291,9 @@ k_reduce(const float *__restrict__ part, int d, int B, int f, const int32_t *__r
     }
     if (!GLUE) return;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        last = atomicAdd(ticket, 1u) == gridDim.x * gridDim.y - 1;
-    }
+    if (threadIdx.x == 0) last = ticket_acq_rel(ticket, 1u) == gridDim.x * gridDim.y - 1;
     __syncthreads();
     if (!last) return;
-    __threadfence();
     for (int bb = warp; bb < B; bb += NW) {
         float t = 0.f;
         for (int k = lane; k < (int)gridDim.x; k += 32) t += __ldcg(sumsq + (size_t)bb * gridDim.x + k);

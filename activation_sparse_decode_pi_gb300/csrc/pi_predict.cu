@@ -147,12 +147,10 @@ k_pred_logits(const uint4 *__restrict__ P2, int r, int f, const float *__restric
     __syncthreads();
     if (threadIdx.x == 0) {
         maskw[blockIdx.x] = word;
-        __threadfence();
-        last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+        last = ticket_acq_rel(ticket, 1u) == gridDim.x - 1;
     }
     __syncthreads();
     if (!last) return;
-    __threadfence();
     __shared__ int wsum[NW];
     compact_words<NW>(maskw, gridDim.x, 0, idx, count, wsum, [] { __syncthreads(); });
     if (threadIdx.x == 0) *ticket = 0u;
@@ -334,13 +332,9 @@ __global__ void __launch_bounds__(FP_NT, 1) k_pred_fused(FusedPredArgs a)
     __syncthreads();
     for (int i = tid; i < w1 - w0; i += FP_NT) a.maskw[w0 + i] = sword[i];
     __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        s_last = atomicAdd(a.ticket, 1u) == (unsigned)P - 1u;
-    }
+    if (tid == 0) s_last = ticket_acq_rel(a.ticket, 1u) == (unsigned)P - 1u;
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     compact_words<FW>(a.maskw, W, 0, a.idx, a.count, wsum, [] { __syncthreads(); });
     if (tid == 0) *a.ticket = 0u;
 }

@@ -56,9 +56,9 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # first 4 layers: dram__bytes_read.sum + dram__bytes_write.sum, mean of two launches
-    # (608.862720 + 23.151872 MB and 613.509120 + 20.072448 MB)
+    # (608.912640 + 23.380992 MB and 613.361920 + 20.183040 MB)
     ("opt175b_d12288_f49152_int4_L96", "decode_stack"): {
-        "bytes_per_layer": (608862720 + 23151872 + 613509120 + 20072448) / 2 / 4, "csrc": "990bc25d717e68c9"},
+        "bytes_per_layer": (608912640 + 23380992 + 613361920 + 20183040) / 2 / 4, "csrc": "b6b93c95275ce51a"},
 }
 
 
