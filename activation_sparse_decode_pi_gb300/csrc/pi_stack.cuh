@@ -818,6 +818,8 @@ __global__ void __launch_bounds__(STACK_NT, 1) k_decode_stack(const StackArgs a)
             // Only the first batch's rows are requested now, the other free slots' rows once they
             // have landed: requested together with everything else (every CTA asks for most of its
             // rows at this point), the first rows land with the bulk of the layer's FFN bytes.
+            // NF must equal the first cold batch's size (nbc below): that batch waits for all of its
+            // slots before the held-back copies are issued.
             const int NF = nh == 0 ? max(1, min(4, SC / 2)) : SC;
             if (nh + cw < nn && cw < SC && cw < NF) {
                 fence_proxy_async_smem();
