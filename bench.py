@@ -56,9 +56,9 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # first 4 layers: dram__bytes_read.sum + dram__bytes_write.sum, mean of two launches
-    # (608.912640 + 23.380992 MB and 613.361920 + 20.183040 MB)
+    # (608.808704 + 23.154432 MB and 613.344000 + 20.373504 MB)
     ("opt175b_d12288_f49152_int4_L96", "decode_stack"): {
-        "bytes_per_layer": (608912640 + 23380992 + 613361920 + 20183040) / 2 / 4, "csrc": "b6b93c95275ce51a"},
+        "bytes_per_layer": (608808704 + 23154432 + 613344000 + 20373504) / 2 / 4, "csrc": "f18cbf211ae24de0"},
 }
 
 
