@@ -65,6 +65,10 @@ def test_step_bytes_accounting():
     w5 = WORKLOADS["opt175b_d12288_f49152_int4_L96"]
     assert bench.neuron_bytes(w5) == 2 * 12288 // 2 + 4 + 2 * (12288 // 128) * 2
     assert bench.kernel_bytes(w5, "pred_logits", 0, 1) == 49152 * 1024 * 2 + 49152 * 4
+    # the one-launch predictor reads both predictor matrices (and the bias); the hot prefix's
+    # P2 rows are not read
+    assert bench.kernel_bytes(w, "pred_fused", 0, 4) == pred
+    assert bench.kernel_bytes(w, "pred_fused", 0, 4, hot=100) == pred - 100 * 1024 * 2
 
 
 def test_ncu_traffic_only_for_the_captured_configuration():
